@@ -1,0 +1,122 @@
+/*
+ * na3d.h - C ABI of the GB300 (sm_103a) forward pass of 3-D neighborhood
+ * attention (NA3D).
+ *
+ * The operation ("[Triton/Gluon] Add 3D neighborhood flash attention
+ * (na3d_flash)", ROCm/aiter pull request 5230):
+ *   - Motivation: the token at grid position (t,h,w) of a video latent
+ *     attends only to its KT x KH x KW neighbours.
+ *   - Technical Details, kernel bullets: windows shift inward at the grid
+ *     borders so that every window holds exactly KT*KH*KW keys; the softmax
+ *     runs online in log2 space.
+ *   - Technical Details, launcher: inputs and output are (B, T, H, W, NH, HD)
+ *     bfloat16, and q arrives already multiplied by head_dim^-0.5.
+ *
+ * On each axis of length N with odd window length K <= N, the query at i uses
+ * keys [s, s+K) with s = min(max(i - K/2, 0), N - K) (integer division).
+ * Scores are q.k accumulated in fp32, the softmax over the window runs in
+ * fp32, the probabilities are rounded to bf16 for the P.V product (fp32
+ * accumulation), and the output is rounded to bf16 (nearest even).
+ *
+ * The library allocates no memory and is safe to call from several host
+ * threads at once. Its only state is a mutex-guarded cache of tiling plans
+ * (keyed by grid and window sizes) and one device word that records a
+ * pipeline-wait timeout (see na3d_device_status).
+ */
+#ifndef NA3D_H
+#define NA3D_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+enum na3d_status {
+    NA3D_OK = 0,
+    NA3D_ERR_NULL = 1,           /* a required pointer is NULL */
+    NA3D_ERR_SHAPE = 2,          /* T, H, W or HD < 1, or B, NH < 0 */
+    NA3D_ERR_KERNEL = 3,         /* a window length is even, < 1, or larger than its axis */
+    NA3D_ERR_HEAD_DIM = 4,       /* HD is not a power of two >= 16 */
+    NA3D_ERR_ALIGN = 5,          /* a tensor pointer is not 16-byte aligned */
+    NA3D_ERR_ALIAS = 6,          /* out overlaps q, k or v */
+    NA3D_ERR_OVERFLOW = 7,       /* a size overflows int64 or a TMA descriptor limit */
+    NA3D_ERR_ARCH = 8,           /* the current device is not compute capability 10.3 */
+    NA3D_ERR_CUDA = 9,           /* a CUDA runtime or driver call failed */
+    NA3D_ERR_DEVICE_TIMEOUT = 10, /* a pipeline wait inside the kernel gave up */
+    NA3D_ERR_UNSUPPORTED = 11    /* valid but not implemented (HD > 256) */
+};
+
+/*
+ * na3d_fwd - out = NA3D(q, k, v) for one bf16 (B,T,H,W,NH,HD) problem.
+ *
+ * q, k, v, out: DEVICE pointers to contiguous row-major bf16 tensors of shape
+ *   (B, T, H, W, NH, HD) (HD fastest), each 16-byte aligned. The caller owns
+ *   all four buffers; the library neither allocates nor frees memory.
+ *   q must already be scaled by HD^-0.5: no scale is applied. q, k and v are
+ *   read only and may alias one another; out must not overlap any of them.
+ * B: batch size, >= 0.  T, H, W: grid sizes, >= 1.  NH: heads, >= 0.
+ *   B == 0 or NH == 0 is an empty problem: the call returns NA3D_OK after
+ *   validation and enqueues nothing.
+ * HD: head dimension, a power of two in [16, 256].
+ * KT, KH, KW: odd window lengths with 1 <= KT <= T, 1 <= KH <= H, 1 <= KW <= W.
+ * stream: a cudaStream_t on the current device (NULL = legacy default stream).
+ *
+ * The call validates its arguments, encodes the TMA descriptors on the host
+ * and enqueues one kernel on `stream`; it returns before the kernel runs. An
+ * argument error returns its code before anything is enqueued (out is not
+ * written). NA3D_ERR_CUDA reports a failed launch or descriptor encoding.
+ * Faults inside the kernel surface through the stream as usual; a pipeline
+ * wait that gives up is reported by na3d_device_status().
+ */
+int na3d_fwd(const void* q, const void* k, const void* v, void* out,
+             int64_t B, int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD,
+             int64_t KT, int64_t KH, int64_t KW, void* stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* na3d_status_string(int status);
+
+/*
+ * How na3d_fwd tiles one (batch, head) slice: queries are cut into bricks of
+ * bt x bh x bw grid positions (at most 128 queries, one tile of the tensor
+ * cores), and each brick streams the union of its queries' windows (its halo)
+ * through shared memory in chunks of cr rows (consecutive h) of cw keys
+ * (consecutive w) in one frame t. The scores of a chunk form one
+ * 128 x n_mma tile.
+ */
+typedef struct na3d_plan_info {
+    int32_t bt, bh, bw;           /* query brick */
+    int32_t cw, cr;               /* chunk: cr rows of cw keys */
+    int32_t n_mma;                /* score-tile width (cr*cw rounded up to 16) */
+    int32_t hd_box;               /* head-dim columns per TMA box (HD or 64) */
+    int32_t stages;               /* K/V shared-memory pipeline depth */
+    int64_t bricks_per_slice;     /* bricks per (batch, head) slice */
+    int64_t chunks_per_slice;     /* chunks per (batch, head) slice */
+    int64_t smem_bytes;           /* dynamic shared memory per CTA */
+} na3d_plan_info;
+
+/*
+ * na3d_plan - the tiling na3d_fwd would use for this problem, computed on the
+ * host without touching a GPU. Arguments as for na3d_fwd; returns the same
+ * argument-validation codes (without the pointer, alignment, alias and device
+ * checks). `info` must not be NULL.
+ */
+int na3d_plan(int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD,
+              int64_t KT, int64_t KH, int64_t KW, na3d_plan_info* info);
+
+/*
+ * na3d_device_status - synchronizes `stream` and reports whether any na3d
+ * kernel on the current device gave up on a pipeline wait (a deadlock guard:
+ * each wait inside the kernel is bounded, and a wait that runs out records a
+ * flag, drains its in-flight copies, frees its tensor memory and returns).
+ * Returns NA3D_ERR_DEVICE_TIMEOUT and clears the flag if it was set,
+ * NA3D_ERR_CUDA if synchronization fails, else NA3D_OK.
+ */
+int na3d_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NA3D_H */

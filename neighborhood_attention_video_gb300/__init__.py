@@ -1,0 +1,124 @@
+"""Python binding of the GB300 NA3D forward library (``libna3d.so``).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/na3d.h``. There is no CPU or
+PyTorch fallback; if the library has not been built, importing works but any
+call raises ``NA3DUnavailable``.
+
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "NA3DError", "NA3DUnavailable", "na3d_fwd", "na3d_status_string", "na3d_plan",
+    "na3d_device_status", "library_path", "load_library", "EXPORTED_SYMBOLS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libna3d.so")
+EXPORTED_SYMBOLS = ("na3d_fwd", "na3d_status_string", "na3d_plan", "na3d_device_status")
+
+NA3D_OK = 0
+_I64 = ctypes.c_int64
+_P = ctypes.c_void_p
+_lib = None
+
+
+class NA3DError(RuntimeError):
+    """A non-zero status returned by the C ABI."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {na3d_status_string(status)} (status {status})")
+
+
+class NA3DUnavailable(RuntimeError):
+    """The CUDA library is missing: build it with ``__graft_entry__.build()``."""
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("bt", ctypes.c_int32), ("bh", ctypes.c_int32), ("bw", ctypes.c_int32),
+                ("cw", ctypes.c_int32), ("cr", ctypes.c_int32), ("n_mma", ctypes.c_int32),
+                ("hd_box", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("bricks_per_slice", ctypes.c_int64), ("chunks_per_slice", ctypes.c_int64),
+                ("smem_bytes", ctypes.c_int64)]
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load_library():
+    """Load ``libna3d.so`` (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise NA3DUnavailable(
+            f"{LIB_PATH} is missing; build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.na3d_fwd.argtypes = [_P, _P, _P, _P] + [_I64] * 9 + [_P]
+    lib.na3d_fwd.restype = ctypes.c_int
+    lib.na3d_status_string.argtypes = [ctypes.c_int]
+    lib.na3d_status_string.restype = ctypes.c_char_p
+    lib.na3d_plan.argtypes = [_I64] * 8 + [ctypes.POINTER(PlanInfo)]
+    lib.na3d_plan.restype = ctypes.c_int
+    lib.na3d_device_status.argtypes = [_P]
+    lib.na3d_device_status.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def na3d_status_string(status: int) -> str:
+    return load_library().na3d_status_string(int(status)).decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def na3d_fwd(q, k, v, out, kernel_size, stream=None) -> None:
+    """out = NA3D(q, k, v) for bf16 CUDA tensors of shape (B, T, H, W, NH, HD).
+
+    ``q`` must already be scaled by HD**-0.5. ``kernel_size`` = (KT, KH, KW),
+    odd. ``out`` is written in place. Runs asynchronously on ``stream``
+    (default: the current torch stream). Raises NA3DError on a bad argument.
+    """
+    import torch
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a bfloat16 CUDA tensor")
+        if t.dim() != 6 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 6-D (B,T,H,W,NH,HD) tensor")
+        if tuple(t.shape) != tuple(q.shape):
+            raise ValueError("q, k, v and out must have the same shape")
+    KT, KH, KW = (int(x) for x in kernel_size)
+    rc = lib.na3d_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                      *[int(x) for x in q.shape], KT, KH, KW, _stream_handle(stream))
+    if rc != NA3D_OK:
+        raise NA3DError(rc, "na3d_fwd")
+
+
+def na3d_plan(T, H, W, NH, HD, KT, KH, KW) -> dict:
+    """The tiling ``na3d_fwd`` uses for this problem (host only, no GPU)."""
+    info = PlanInfo()
+    rc = load_library().na3d_plan(T, H, W, NH, HD, KT, KH, KW, ctypes.byref(info))
+    if rc != NA3D_OK:
+        raise NA3DError(rc, "na3d_plan")
+    return {name: getattr(info, name) for name, _ in PlanInfo._fields_}
+
+
+def na3d_device_status(stream=None) -> int:
+    """Synchronize ``stream``; NA3D_ERR_DEVICE_TIMEOUT if a kernel wait gave up."""
+    return int(load_library().na3d_device_status(_stream_handle(stream)))

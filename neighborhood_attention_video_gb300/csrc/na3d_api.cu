@@ -1,0 +1,280 @@
+// C ABI of the NA3D forward pass: argument validation, the brick/chunk
+// planner, TMA descriptor encoding and the launch. Declared in include/na3d.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "na3d.h"
+#include "na3d_kernel.cuh"
+
+namespace {
+
+using na3d::KernelParams;
+using na3d::VariantInfo;
+
+// ------------------------------------------------------------------ validation
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+bool mul_ok(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a, b, r); }
+
+int validate_shape(int64_t B, int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT,
+                   int64_t KH, int64_t KW) {
+    if (B < 0 || NH < 0 || T < 1 || H < 1 || W < 1 || HD < 1) return NA3D_ERR_SHAPE;
+    const int64_t ks[3] = {KT, KH, KW}, ns[3] = {T, H, W};
+    for (int a = 0; a < 3; ++a)
+        if (ks[a] < 1 || (ks[a] & 1) == 0 || ks[a] > ns[a]) return NA3D_ERR_KERNEL;
+    if (!is_pow2(HD) || HD < 16) return NA3D_ERR_HEAD_DIM;
+    // element count and byte size of one tensor must fit int64; TMA limits:
+    // every global dimension < 2^32, every stride < 2^40 bytes.
+    int64_t n = 1;
+    const int64_t dims[6] = {B > 0 ? B : 1, T, H, W, NH > 0 ? NH : 1, HD};
+    for (int i = 0; i < 6; ++i)
+        if (!mul_ok(n, dims[i], &n)) return NA3D_ERR_OVERFLOW;
+    if (!mul_ok(n, 2, &n)) return NA3D_ERR_OVERFLOW;
+    if (NH * HD >= (int64_t(1) << 32) || W >= (int64_t(1) << 31) || H >= (int64_t(1) << 31) ||
+        T >= (int64_t(1) << 31) || B >= (int64_t(1) << 31))
+        return NA3D_ERR_OVERFLOW;
+    if (n / dims[0] >= (int64_t(1) << 40)) return NA3D_ERR_OVERFLOW;  // batch stride in bytes
+    if (HD > 256) return NA3D_ERR_UNSUPPORTED;
+    return NA3D_OK;
+}
+
+// ------------------------------------------------------------------ planner
+
+int64_t win_start(int64_t i, int64_t K, int64_t N) {
+    int64_t s = i - K / 2;
+    if (s < 0) s = 0;
+    if (s > N - K) s = N - K;
+    return s;
+}
+
+// Sum over the bricks of one axis of ceil(extent / unit), where extent is the
+// length of the union of the windows of the brick's queries (unit 1: the
+// union length itself). Also returns the number of bricks.
+int64_t axis_sum(int64_t N, int64_t K, int64_t b, int64_t unit, int64_t* nbricks) {
+    int64_t sum = 0, cnt = 0;
+    for (int64_t p0 = 0; p0 < N; p0 += b, ++cnt) {
+        const int64_t last = (p0 + b < N ? p0 + b : N) - 1;
+        const int64_t ext = win_start(last, K, N) + K - win_start(p0, K, N);
+        sum += (ext + unit - 1) / unit;
+    }
+    *nbricks = cnt;
+    return sum;
+}
+
+struct Plan {
+    int bt = 0, bh = 0, bw = 0, cw = 0, cr = 0, n_mma = 0;
+    int64_t bricks = 0, chunks = 0;
+    double cost = 0;
+};
+
+// Costs in units of score columns of a 128-row tile: every chunk costs its
+// tile width (tensor-core and exp work) plus a fixed overhead (barriers, mask
+// set-up, MMA issue); every brick adds the epilogue and its Q load.
+constexpr double kChunkOverhead = 24.0;
+constexpr double kBrickOverhead = 96.0;
+
+Plan make_plan(int64_t T, int64_t H, int64_t W, int64_t KT, int64_t KH, int64_t KW, int ncap) {
+    Plan best;
+    for (int64_t bw = 1; bw <= (W < 128 ? W : 128); ++bw) {
+        const int64_t ew = (bw + KW - 1 < W) ? bw + KW - 1 : W;   // widest W union
+        const int64_t cw = ew > ncap ? ncap : ew;
+        int64_t nbw;
+        const int64_t sw = axis_sum(W, KW, bw, cw, &nbw);
+        for (int64_t bh = 1; bh <= H && bw * bh <= 128; ++bh) {
+            const int64_t eh = (bh + KH - 1 < H) ? bh + KH - 1 : H;
+            int64_t cr = ew > ncap ? 1 : ncap / cw;
+            if (cr > eh) cr = eh;
+            const int64_t n_mma = (cr * cw + 15) / 16 * 16;
+            int64_t nbh;
+            const int64_t sh = axis_sum(H, KH, bh, cr, &nbh);
+            for (int64_t bt = 1; bt <= T && bw * bh * bt <= 128; ++bt) {
+                int64_t nbt;
+                const int64_t st = axis_sum(T, KT, bt, 1, &nbt);
+                const int64_t chunks = st * sh * sw;
+                const int64_t bricks = nbt * nbh * nbw;
+                const double cost = double(chunks) * (double(n_mma) + kChunkOverhead) +
+                                    double(bricks) * kBrickOverhead;
+                const bool better =
+                    best.bt == 0 || cost < best.cost - 1e-9 ||
+                    (cost < best.cost + 1e-9 && bw * bh * bt > int64_t(best.bw) * best.bh * best.bt);
+                if (better) {
+                    best.bt = int(bt); best.bh = int(bh); best.bw = int(bw);
+                    best.cw = int(cw); best.cr = int(cr); best.n_mma = int(n_mma);
+                    best.bricks = bricks; best.chunks = chunks; best.cost = cost;
+                }
+            }
+        }
+    }
+    return best;
+}
+
+// Plans depend only on the grid, the window and the score-tile cap; they are
+// cached (bounded, mutex-guarded) because the search takes ~0.1 ms.
+Plan cached_plan(int64_t T, int64_t H, int64_t W, int64_t KT, int64_t KH, int64_t KW, int ncap) {
+    using Key = std::tuple<int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int>;
+    static std::mutex mu;
+    static std::map<Key, Plan> cache;
+    const Key key{T, H, W, KT, KH, KW, ncap};
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    Plan pl = make_plan(T, H, W, KT, KH, KW, ncap);
+    std::lock_guard<std::mutex> g(mu);
+    if (cache.size() >= 1024) cache.clear();
+    cache.emplace(key, pl);
+    return pl;
+}
+
+// ------------------------------------------------------------------ TMA descriptors
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// The (B,T,H,W,NH,HD) tensor viewed as 5-D (NH*HD, W, H, T, B): a box of
+// {hd_box, bx, by, bz, 1} at x = head*HD + column picks one head's rows.
+bool encode_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t H, int64_t W,
+                int64_t NH, int64_t HD, int hd_box, int bx, int by, int bz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[5] = {cuuint64_t(NH * HD), cuuint64_t(W), cuuint64_t(H), cuuint64_t(T),
+                                cuuint64_t(B)};
+    const cuuint64_t row = cuuint64_t(NH * HD * 2);
+    const cuuint64_t strides[4] = {row, row * W, row * W * H, row * W * H * T};
+    const cuuint32_t box[5] = {cuuint32_t(hd_box), cuuint32_t(bx), cuuint32_t(by), cuuint32_t(bz), 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUtensorMapSwizzle swz = hd_box == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : hd_box == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                  : CU_TENSOR_MAP_SWIZZLE_32B;
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, const void* b, int64_t bytes) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + uintptr_t(bytes) && y < x + uintptr_t(bytes);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* na3d_status_string(int status) {
+    switch (status) {
+        case NA3D_OK: return "NA3D_OK";
+        case NA3D_ERR_NULL: return "NA3D_ERR_NULL: a required pointer is NULL";
+        case NA3D_ERR_SHAPE: return "NA3D_ERR_SHAPE: T, H, W, HD must be >= 1 and B, NH >= 0";
+        case NA3D_ERR_KERNEL: return "NA3D_ERR_KERNEL: window lengths must be odd and within 1..axis length";
+        case NA3D_ERR_HEAD_DIM: return "NA3D_ERR_HEAD_DIM: head dimension must be a power of two >= 16";
+        case NA3D_ERR_ALIGN: return "NA3D_ERR_ALIGN: tensor pointers must be 16-byte aligned";
+        case NA3D_ERR_ALIAS: return "NA3D_ERR_ALIAS: out overlaps q, k or v";
+        case NA3D_ERR_OVERFLOW: return "NA3D_ERR_OVERFLOW: sizes exceed int64 or TMA descriptor limits";
+        case NA3D_ERR_ARCH: return "NA3D_ERR_ARCH: the current device is not sm_103 (GB300)";
+        case NA3D_ERR_CUDA: return "NA3D_ERR_CUDA: a CUDA call failed";
+        case NA3D_ERR_DEVICE_TIMEOUT: return "NA3D_ERR_DEVICE_TIMEOUT: a pipeline wait in the kernel gave up";
+        case NA3D_ERR_UNSUPPORTED: return "NA3D_ERR_UNSUPPORTED: head dimension above 256 is not implemented";
+        default: return "unknown na3d status";
+    }
+}
+
+int na3d_plan(int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT, int64_t KH,
+              int64_t KW, na3d_plan_info* info) {
+    if (!info) return NA3D_ERR_NULL;
+    const int rc = validate_shape(1, T, H, W, NH, HD, KT, KH, KW);
+    if (rc != NA3D_OK) return rc;
+    VariantInfo vi;
+    if (!na3d::variant_info(int(HD), &vi)) return NA3D_ERR_UNSUPPORTED;
+    const Plan pl = cached_plan(T, H, W, KT, KH, KW, vi.ncap);
+    info->bt = pl.bt; info->bh = pl.bh; info->bw = pl.bw;
+    info->cw = pl.cw; info->cr = pl.cr; info->n_mma = pl.n_mma;
+    info->hd_box = vi.hd_box; info->stages = vi.stages;
+    info->bricks_per_slice = pl.bricks;
+    info->chunks_per_slice = pl.chunks;
+    info->smem_bytes = vi.smem;
+    return NA3D_OK;
+}
+
+int na3d_fwd(const void* q, const void* k, const void* v, void* out, int64_t B, int64_t T,
+             int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT, int64_t KH, int64_t KW,
+             void* stream) {
+    if (!q || !k || !v || !out) return NA3D_ERR_NULL;
+    int rc = validate_shape(B, T, H, W, NH, HD, KT, KH, KW);
+    if (rc != NA3D_OK) return rc;
+    const void* ptrs[4] = {q, k, v, out};
+    for (const void* p : ptrs)
+        if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return NA3D_ERR_ALIGN;
+    const int64_t bytes = B * T * H * W * NH * HD * 2;
+    if (bytes == 0) return NA3D_OK;  // B == 0 or NH == 0: nothing to compute
+    if (overlaps(out, q, bytes) || overlaps(out, k, bytes) || overlaps(out, v, bytes))
+        return NA3D_ERR_ALIAS;
+
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return NA3D_ERR_CUDA;
+    if (major != 10 || minor != 3) return NA3D_ERR_ARCH;
+
+    VariantInfo vi;
+    if (!na3d::variant_info(int(HD), &vi)) return NA3D_ERR_UNSUPPORTED;
+    const Plan pl = cached_plan(T, H, W, KT, KH, KW, vi.ncap);
+
+    KernelParams kp;
+    kp.B = int32_t(B); kp.T = int32_t(T); kp.H = int32_t(H); kp.W = int32_t(W); kp.NH = int32_t(NH);
+    kp.KT = int32_t(KT); kp.KH = int32_t(KH); kp.KW = int32_t(KW);
+    kp.bt = pl.bt; kp.bh = pl.bh; kp.bw = pl.bw;
+    kp.nbt = int32_t((T + pl.bt - 1) / pl.bt);
+    kp.nbh = int32_t((H + pl.bh - 1) / pl.bh);
+    kp.nbw = int32_t((W + pl.bw - 1) / pl.bw);
+    kp.cw = pl.cw; kp.cr = pl.cr; kp.n_mma = pl.n_mma;
+    const int64_t units = B * int64_t(kp.nbt) * kp.nbh * kp.nbw * NH;
+    if (units >= (int64_t(1) << 31)) return NA3D_ERR_OVERFLOW;
+    kp.n_units = int32_t(units);
+    kp.out = static_cast<uint16_t*>(out);
+
+    CUtensorMap tq, tk, tv;
+    if (!encode_map(&tq, q, B, T, H, W, NH, HD, vi.hd_box, pl.bw, pl.bh, pl.bt) ||
+        !encode_map(&tk, k, B, T, H, W, NH, HD, vi.hd_box, pl.cw, pl.cr, 1) ||
+        !encode_map(&tv, v, B, T, H, W, NH, HD, vi.hd_box, pl.cw, pl.cr, 1))
+        return NA3D_ERR_CUDA;
+
+    const int grid = int(units < sms ? units : sms);
+    if (na3d::launch_fwd(int(HD), tq, tk, tv, kp, grid, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return NA3D_ERR_CUDA;
+    return NA3D_OK;
+}
+
+int na3d_device_status(void* stream) {
+    unsigned int flag = 0;
+    if (na3d::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &flag) != cudaSuccess)
+        return NA3D_ERR_CUDA;
+    return flag ? NA3D_ERR_DEVICE_TIMEOUT : NA3D_OK;
+}
+
+}  // extern "C"

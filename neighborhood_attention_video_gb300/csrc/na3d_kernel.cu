@@ -1,0 +1,585 @@
+// NA3D forward on GB300 (sm_103a): persistent, warp-specialised kernel.
+//
+// The operation ("[Triton/Gluon] Add 3D neighborhood flash attention
+// (na3d_flash)", ROCm/aiter pull request 5230, Motivation and Technical
+// Details): each query (t,h,w) of a (B,T,H,W,NH,HD) bf16 tensor attends to the
+// KT x KH x KW keys of its inward-shifted window; q is pre-scaled; the softmax
+// is online and runs in log2 space with the log2(e) factor folded into the
+// exponent; the output is bf16 in the input layout.
+//
+// Work decomposition. One work unit is one query brick (bt x bh x bw <= 128
+// grid positions) of one (batch, head). Its keys are the union of its
+// queries' windows (the halo), a box that is streamed through shared memory
+// in chunks: a chunk is cr consecutive rows (h) of cw consecutive keys (w) in
+// one frame (t), loaded with one TMA box per 64 head-dim columns. Queries are
+// the M = 128 rows of every tensor-core tile; a chunk's keys are its N columns.
+//
+// Roles (192 threads, one CTA per SM, loop over units):
+//   warp 0      TMA producer: Q brick once per unit, K and V per chunk into a
+//               ring of `NS` stages.
+//   warp 1      tensor-core issuer: S = Q K^T into one of two TMEM score
+//               buffers, then O += P V into the TMEM output accumulator; owns
+//               the tensor-memory allocation.
+//   warps 2..5  softmax: one query row per thread (TMEM lane), window mask,
+//               running max / sum in log2 space, P as bf16 into shared memory,
+//               occasional O rescale, and the epilogue O / l -> bf16 -> HBM.
+//
+// Every pipeline wait is bounded: a wait that runs out sets a device flag, all
+// roles drop out of their loops, in-flight copies and MMAs are drained, and
+// the tensor memory is freed before the CTA exits.
+#include <cuda_bf16.h>
+
+#include "na3d_kernel.cuh"
+#include "sm103_ptx.cuh"
+
+namespace na3d {
+
+__device__ unsigned int g_na3d_timeout_flag = 0;
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
+constexpr uint64_t kDrainLimitNs = 500000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+// A new running maximum replaces the reference maximum only when it exceeds it
+// by more than this (log2 units): probabilities stay <= 2^8 and the O rescale
+// (a TMEM round trip) is rare.
+constexpr float kRescaleThreshold = 8.0f;
+constexpr int kThreads = 192;
+constexpr int kMinSmem = 120 * 1024;  // forces one CTA per SM (each CTA takes all 512 TMEM columns)
+
+template <int HD_, int NCAP_, int NS_, int NQ_>
+struct Cfg {
+    static constexpr int HD = HD_, NCAP = NCAP_, NS = NS_, NQ = NQ_;
+    static constexpr int HDB = HD < 64 ? HD : 64;   // head-dim columns per TMA box / smem row
+    static constexpr int NREG = HD / HDB;           // boxes (smem regions) per tile
+    static constexpr int ROWB = HDB * 2;            // bytes per smem row
+    static constexpr uint32_t SWZ = HDB == 64 ? kSwizzle128B : (HDB == 32 ? kSwizzle64B : kSwizzle32B);
+    static constexpr int SBO = 8 * ROWB;            // stride between 8-row core groups
+    static constexpr int Q_REG = 128 * ROWB;
+    static constexpr int Q_TILE = NREG * Q_REG;
+    static constexpr int KV_REG = NCAP * ROWB;
+    static constexpr int KV_TILE = NREG * KV_REG;
+    static constexpr int P_REG = 128 * 128;         // 64 bf16 key columns x 128 rows
+    static constexpr int P_TILE = (NCAP / 64) * P_REG;
+    static constexpr int NW = NCAP / 32;            // 32-column words per score row
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
+    static constexpr int OFF_V = OFF_K + NS * KV_TILE;
+    static constexpr int OFF_P = OFF_V + NS * KV_TILE;
+    static constexpr int OFF_BAR = OFF_P + 2 * P_TILE;
+    // barrier indices
+    static constexpr int B_QFULL = 0, B_QEMPTY = NQ, B_KVFULL = 2 * NQ, B_KVEMPTY = 2 * NQ + NS;
+    static constexpr int B_SFULL = 2 * NQ + 2 * NS, B_SEMPTY = B_SFULL + 2, B_PFULL = B_SFULL + 4,
+                         B_PVDONE = B_SFULL + 6, B_OFULL = B_SFULL + 8, B_OEMPTY = B_SFULL + 9,
+                         B_DRAIN = B_SFULL + 10, NBAR = B_SFULL + 11;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    static constexpr int SMEM_ALLOC =
+        (SMEM_USED + 1024) > kMinSmem ? (SMEM_USED + 1024) : kMinSmem;
+    static constexpr uint32_t TM_S = 0;            // score buffers: [0, NCAP), [NCAP, 2 NCAP)
+    static constexpr uint32_t TM_O = 2 * NCAP;     // output accumulator: HD columns
+    static constexpr uint32_t TM_COLS = 512;
+    static_assert(TM_O + HD <= TM_COLS, "TMEM budget");
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static_assert(NCAP == 64 || NCAP == 128, "score tile width");
+    static_assert(NS >= 2, "the K/V ring needs two stages to avoid a producer/MMA cycle");
+};
+
+// ------------------------------------------------------------------ geometry
+
+__device__ __forceinline__ int win_start(int i, int K, int N) {
+    int s = i - (K >> 1);
+    s = s < 0 ? 0 : s;
+    return s > N - K ? N - K : s;
+}
+
+struct Unit {
+    int b, n, t0, h0, w0;
+    int lo_t, lo_h, lo_w;
+    int n_hc, n_wc, nch;
+};
+
+__device__ __forceinline__ Unit unit_of(const KernelParams& p, int u) {
+    Unit U;
+    U.n = u % p.NH;
+    u /= p.NH;
+    const int iw = u % p.nbw;
+    u /= p.nbw;
+    const int ih = u % p.nbh;
+    u /= p.nbh;
+    const int it = u % p.nbt;
+    U.b = u / p.nbt;
+    U.t0 = it * p.bt;
+    U.h0 = ih * p.bh;
+    U.w0 = iw * p.bw;
+    U.lo_t = win_start(U.t0, p.KT, p.T);
+    U.lo_h = win_start(U.h0, p.KH, p.H);
+    U.lo_w = win_start(U.w0, p.KW, p.W);
+    const int hi_t = win_start(min(U.t0 + p.bt, p.T) - 1, p.KT, p.T) + p.KT;
+    const int hi_h = win_start(min(U.h0 + p.bh, p.H) - 1, p.KH, p.H) + p.KH;
+    const int hi_w = win_start(min(U.w0 + p.bw, p.W) - 1, p.KW, p.W) + p.KW;
+    U.n_hc = (hi_h - U.lo_h + p.cr - 1) / p.cr;
+    U.n_wc = (hi_w - U.lo_w + p.cw - 1) / p.cw;
+    U.nch = (hi_t - U.lo_t) * U.n_hc * U.n_wc;
+    return U;
+}
+
+// Chunk order inside a unit: w-segment fastest, then h-row group, then frame.
+struct ChunkCursor {
+    int kt, hc, wc;
+    __device__ __forceinline__ void advance(const Unit& U) {
+        if (++wc == U.n_wc) {
+            wc = 0;
+            if (++hc == U.n_hc) {
+                hc = 0;
+                ++kt;
+            }
+        }
+    }
+};
+
+// bits [a, b) of a 128-bit mask held in four words (0 <= a, b <= 128)
+__device__ __forceinline__ void bit_range128(uint32_t m[4], int a, int b) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const int lo = max(a - 32 * w, 0), hi = min(b - 32 * w, 32);
+        m[w] = hi > lo ? static_cast<uint32_t>(((1ull << (hi - lo)) - 1ull) << lo) : 0u;
+    }
+}
+
+// ------------------------------------------------------------------ waits
+
+struct Sync {
+    uint32_t bar0;                     // smem address of barrier 0
+    volatile uint32_t* abort_flag;     // smem, shared by all roles
+    __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * i; }
+
+    // Wait for a barrier phase; false once this CTA has given up.
+    __device__ __forceinline__ bool wait(uint32_t b, uint32_t parity) const {
+        if (mbar_try_wait(b, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 1;; ++it) {
+            if (mbar_try_wait(b, parity)) return true;
+            if ((it & 1023u) == 0u) {
+                if (*abort_flag) return false;
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    *abort_flag = 1u;
+                    atomicOr(&g_na3d_timeout_flag, 1u);
+                    return false;
+                }
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------------ roles
+
+template <class C>
+__device__ void producer_role(const KernelParams& p, const CUtensorMap* tq, const CUtensorMap* tk,
+                              const CUtensorMap* tv, const Sync& sy, uint32_t base) {
+    uint32_t g = 0, ul = 0, nq = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++ul) {
+        const Unit U = unit_of(p, u);
+        const int xq = U.n * C::HD;
+        ChunkCursor cur{U.lo_t, 0, 0};
+        for (int c = 0; c < U.nch; ++c, ++g) {
+            const uint32_t st = g % C::NS;
+            if (!sy.wait(sy.bar(C::B_KVEMPTY + st), ((g / C::NS) & 1u) ^ 1u)) { ok = false; break; }
+            const uint32_t full = sy.bar(C::B_KVFULL + st);
+            mbar_arrive_expect_tx(full, 2u * C::NREG * C::ROWB * p.cw * p.cr);
+            const int kh0 = U.lo_h + cur.hc * p.cr, kw0 = U.lo_w + cur.wc * p.cw;
+#pragma unroll
+            for (int r = 0; r < C::NREG; ++r) {
+                tma_load_5d(base + C::OFF_K + st * C::KV_TILE + r * C::KV_REG, tk, full,
+                            xq + r * C::HDB, kw0, kh0, cur.kt, U.b);
+                tma_load_5d(base + C::OFF_V + st * C::KV_TILE + r * C::KV_REG, tv, full,
+                            xq + r * C::HDB, kw0, kh0, cur.kt, U.b);
+            }
+            cur.advance(U);
+            if (c == 0) {  // the Q brick goes right behind the unit's first K/V chunk
+                const uint32_t qb = ul % C::NQ;
+                if (!sy.wait(sy.bar(C::B_QEMPTY + qb), ((ul / C::NQ) & 1u) ^ 1u)) { ok = false; ++g; break; }
+                const uint32_t qf = sy.bar(C::B_QFULL + qb);
+                mbar_arrive_expect_tx(qf, C::NREG * C::ROWB * p.bt * p.bh * p.bw);
+#pragma unroll
+                for (int r = 0; r < C::NREG; ++r)
+                    tma_load_5d(base + C::OFF_Q + qb * C::Q_TILE + r * C::Q_REG, tq, qf,
+                                xq + r * C::HDB, U.w0, U.h0, U.t0, U.b);
+                ++nq;
+            }
+        }
+    }
+    // Drain: every issued load must land before the CTA may exit.
+    for (uint32_t s = 0; s < C::NS; ++s) {
+        const uint32_t fills = g / C::NS + (s < g % C::NS ? 1u : 0u);
+        if (fills) mbar_wait_bounded(sy.bar(C::B_KVFULL + s), (fills - 1u) & 1u, kDrainLimitNs);
+    }
+    for (uint32_t s = 0; s < C::NQ; ++s) {
+        const uint32_t fills = nq / C::NQ + (s < nq % C::NQ ? 1u : 0u);
+        if (fills) mbar_wait_bounded(sy.bar(C::B_QFULL + s), (fills - 1u) & 1u, kDrainLimitNs);
+    }
+}
+
+template <class C>
+__device__ void mma_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem) {
+    const uint32_t idesc_s = make_idesc_bf16(128, p.n_mma, 0, 0);
+    const uint32_t idesc_o = make_idesc_bf16(128, C::HD, 0, 1);
+    uint32_t g = 0, ul = 0;
+
+    // O += P_g V_g; `first` marks the unit's first product (overwrites O).
+    auto issue_pv = [&](uint32_t gp, bool first) -> bool {
+        const uint32_t sb = gp & 1u, st = gp % C::NS;
+        if (first && !sy.wait(sy.bar(C::B_OEMPTY), (ul & 1u) ^ 1u)) return false;
+        if (!sy.wait(sy.bar(C::B_PFULL + sb), (gp >> 1) & 1u)) return false;
+        tc_fence_after();
+        const uint32_t pa = base + C::OFF_P + sb * C::P_TILE;
+        const uint32_t va = base + C::OFF_V + st * C::KV_TILE;
+        const int ksteps = p.n_mma >> 4;
+        for (int kk = 0; kk < ksteps; ++kk) {
+            const uint64_t ad = make_smem_desc(pa + (kk >> 2) * C::P_REG + (kk & 3) * 32, 16, 1024,
+                                               kSwizzle128B);
+            const uint64_t bd = make_smem_desc(va + kk * 16 * C::ROWB, C::KV_REG, C::SBO, C::SWZ);
+            umma_bf16_ss(tmem + C::TM_O, ad, bd, idesc_o, (first && kk == 0) ? 0u : 1u);
+        }
+        umma_commit(sy.bar(C::B_PVDONE + sb));
+        umma_commit(sy.bar(C::B_KVEMPTY + st));
+        return true;
+    };
+
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++ul) {
+        const Unit U = unit_of(p, u);
+        const uint32_t qb = ul % C::NQ;
+        if (!sy.wait(sy.bar(C::B_QFULL + qb), (ul / C::NQ) & 1u)) break;
+        tc_fence_after();
+        const uint32_t qa = base + C::OFF_Q + qb * C::Q_TILE;
+        for (int c = 0; c < U.nch; ++c, ++g) {
+            const uint32_t st = g % C::NS, sb = g & 1u;
+            if (!sy.wait(sy.bar(C::B_KVFULL + st), (g / C::NS) & 1u)) { ok = false; break; }
+            if (!sy.wait(sy.bar(C::B_SEMPTY + sb), ((g >> 1) & 1u) ^ 1u)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t ka = base + C::OFF_K + st * C::KV_TILE;
+#pragma unroll
+            for (int kk = 0; kk < C::HD / 16; ++kk) {
+                const int reg = kk / (C::HDB / 16), sub = kk % (C::HDB / 16);
+                const uint64_t ad = make_smem_desc(qa + reg * C::Q_REG + sub * 32, 16, C::SBO, C::SWZ);
+                const uint64_t bd = make_smem_desc(ka + reg * C::KV_REG + sub * 32, 16, C::SBO, C::SWZ);
+                umma_bf16_ss(tmem + C::TM_S + sb * C::NCAP, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(sy.bar(C::B_SFULL + sb));
+            if (c == U.nch - 1) umma_commit(sy.bar(C::B_QEMPTY + qb));
+            if (c > 0 && !issue_pv(g - 1, c == 1)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (!issue_pv(g - 1, U.nch == 1)) break;
+        umma_commit(sy.bar(C::B_OFULL));
+    }
+    // Drain: all MMAs issued by this thread complete before TMEM is freed.
+    umma_commit(sy.bar(C::B_DRAIN));
+    mbar_wait_bounded(sy.bar(C::B_DRAIN), 0, kDrainLimitNs);
+}
+
+template <class C>
+__device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem,
+                             int warp, int lane) {
+    const int quarter = warp & 3;               // TMEM lanes this warp may access
+    const int r = quarter * 32 + lane;          // tile row = query of the brick
+    const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int M = p.bt * p.bh * p.bw;
+    const int iw = r % p.bw, ih = (r / p.bw) % p.bh, it = r / (p.bw * p.bh);
+    const uint32_t p_row_off = (r >> 3) * 1024 + (r & 7) * 128;
+    uint32_t g = 0, ul = 0;
+
+    for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++ul) {
+        const Unit U = unit_of(p, u);
+        const int t = U.t0 + it, h = U.h0 + ih, w = U.w0 + iw;
+        const bool valid = r < M && t < p.T && h < p.H && w < p.W;
+        const int sT = win_start(t, p.KT, p.T), sH = win_start(h, p.KH, p.H),
+                  sW = win_start(w, p.KW, p.W);
+        // Column pattern of this row's window inside one chunk (when a chunk
+        // holds several h-rows, the whole W extent of the halo fits in cw).
+        uint32_t rowpat[4] = {0u, 0u, 0u, 0u};
+        if (p.cr > 1) {
+            const int c0 = max(sW - U.lo_w, 0), c1 = min(sW + p.KW - U.lo_w, p.cw);
+            for (int i = 0; i < p.cr; ++i) {
+                uint32_t tmp[4];
+                bit_range128(tmp, i * p.cw + c0, i * p.cw + c1);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) rowpat[q] |= tmp[q];
+            }
+        }
+        float m_ref = -INFINITY;   // reference maximum, log2 units
+        float l = 0.f;             // running sum of the bf16-rounded probabilities
+        ChunkCursor cur{U.lo_t, 0, 0};
+
+        for (int c = 0; c < U.nch; ++c, ++g) {
+            const uint32_t sb = g & 1u;
+            if (!sy.wait(sy.bar(C::B_SFULL + sb), (g >> 1) & 1u)) return;
+            tc_fence_after();
+            float s[C::NCAP];
+#pragma unroll
+            for (int q = 0; q < C::NW; ++q)
+                if (q * 32 < p.n_mma) tmem_ld32(t_row + C::TM_S + sb * C::NCAP + q * 32, s + 32 * q);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(sy.bar(C::B_SEMPTY + sb));
+
+            // window mask of this row over the chunk's cr x cw keys
+            uint32_t m[4] = {0u, 0u, 0u, 0u};
+            const int kh0 = U.lo_h + cur.hc * p.cr, kw0 = U.lo_w + cur.wc * p.cw;
+            if (valid && static_cast<unsigned>(cur.kt - sT) < static_cast<unsigned>(p.KT)) {
+                const int i0 = max(sH - kh0, 0), i1 = min(sH + p.KH - kh0, p.cr);
+                const int c0 = max(sW - kw0, 0), c1 = min(sW + p.KW - kw0, p.cw);
+                if (i0 < i1 && c0 < c1) {
+                    if (p.cr == 1) {
+                        bit_range128(m, c0, c1);
+                    } else {
+                        bit_range128(m, i0 * p.cw, i1 * p.cw);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) m[q] &= rowpat[q];
+                    }
+                }
+            }
+            cur.advance(U);
+
+            bool live[C::NW];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < C::NW; ++q) {
+                live[q] = (q * 32 < p.n_mma) && __any_sync(0xffffffffu, m[q] != 0u);
+                if (live[q]) {
+#pragma unroll
+                    for (int b = 0; b < 32; ++b) {
+                        const float x = ((m[q] >> b) & 1u) ? s[32 * q + b] : -INFINITY;
+                        s[32 * q + b] = x;
+                        mx = fmaxf(mx, x);
+                    }
+                }
+            }
+            const float mx2 = mx * kLog2e;
+            float alpha = 1.f;
+            bool rescale = false;
+            if (mx2 > m_ref + kRescaleThreshold) {
+                if (m_ref != -INFINITY) {
+                    alpha = ex2_approx(m_ref - mx2);
+                    rescale = true;
+                }
+                m_ref = mx2;
+            }
+            const float moff = m_ref == -INFINITY ? 0.f : m_ref;
+            l *= alpha;
+
+            // P buffer `sb` is free once the product two chunks back is done.
+            if (!sy.wait(sy.bar(C::B_PVDONE + sb), ((g >> 1) & 1u) ^ 1u)) return;
+            const uint32_t prow = base + C::OFF_P + sb * C::P_TILE + p_row_off;
+            float lsum = 0.f;
+#pragma unroll
+            for (int q = 0; q < C::NW; ++q) {
+                if (q * 32 < p.n_mma) {
+                    uint32_t pk[16];
+                    if (live[q]) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float a = ex2_approx(fmaf(s[32 * q + 2 * j], kLog2e, -moff));
+                            const float bb = ex2_approx(fmaf(s[32 * q + 2 * j + 1], kLog2e, -moff));
+                            pk[j] = pack_bf16x2(a, bb);
+                            lsum += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) pk[j] = 0u;
+                    }
+#pragma unroll
+                    for (int cq = 0; cq < 4; ++cq) {
+                        const int chunk16 = q * 4 + cq;          // 8 keys = 16 bytes
+                        const uint32_t addr = prow + (chunk16 >> 3) * C::P_REG +
+                                              (((chunk16 & 7) ^ (r & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                                     "r"(pk[4 * cq]), "r"(pk[4 * cq + 1]), "r"(pk[4 * cq + 2]),
+                                     "r"(pk[4 * cq + 3])
+                                     : "memory");
+                    }
+                }
+            }
+            l += lsum;
+            fence_proxy_async_smem();
+
+            if (__any_sync(0xffffffffu, rescale)) {
+                // the previous product must have landed in O before it is scaled
+                const uint32_t gp = g - 1;
+                if (!sy.wait(sy.bar(C::B_PVDONE + (gp & 1u)), (gp >> 1) & 1u)) return;
+                tc_fence_after();
+                const float a = rescale ? alpha : 1.f;
+#pragma unroll 1
+                for (int q = 0; q < C::HD / 32; ++q) {
+                    float o[32];
+                    tmem_ld32(t_row + C::TM_O + q * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] *= a;
+                    tmem_st32(t_row + C::TM_O + q * 32, o);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            mbar_arrive(sy.bar(C::B_PFULL + sb));
+        }
+
+        // epilogue: O / l -> bf16 -> global
+        if (!sy.wait(sy.bar(C::B_OFULL), ul & 1u)) return;
+        tc_fence_after();
+        const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
+        const int64_t tok = ((static_cast<int64_t>(U.b) * p.T + t) * p.H + h) * p.W + w;
+        uint16_t* orow = p.out + (tok * p.NH + U.n) * C::HD;
+#pragma unroll 1
+        for (int q = 0; q < C::HD / 32; ++q) {
+            float o[32];
+            tmem_ld32(t_row + C::TM_O + q * 32, o);
+            tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(o[2 * j] * inv, o[2 * j + 1] * inv);
+            if (valid) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(sy.bar(C::B_OEMPTY));
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int HD, int NCAP, int NS, int NQ>
+__global__ void __launch_bounds__(kThreads, 1)
+na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
+    using C = Cfg<HD, NCAP, NS, NQ>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // Zero all tiles once: pad rows of Q and K/V tiles are never written by
+    // TMA and must hold finite values (a zero probability times NaN is NaN).
+    {
+        uint4* z = reinterpret_cast<uint4*>(base_ptr);
+        for (int i = threadIdx.x; i < C::OFF_BAR / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_MISC);
+    Sync sy{base + C::OFF_BAR, misc + 1};
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NBAR; ++i) {
+            uint32_t cnt = 1;
+            if ((i >= C::B_SEMPTY && i < C::B_SEMPTY + 2) || (i >= C::B_PFULL && i < C::B_PFULL + 2) ||
+                i == C::B_OEMPTY)
+                cnt = 128;
+            mbar_init(sy.bar(i), cnt);
+        }
+        misc[1] = 0u;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(base + C::OFF_MISC, C::TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp == 0) {
+        if (lane == 0) producer_role<C>(p, &tm_q, &tm_k, &tm_v, sy, base);
+    } else if (warp == 1) {
+        if (lane == 0) mma_role<C>(p, sy, base, tmem);
+    } else {
+        softmax_role<C>(p, sy, base, tmem, warp, lane);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+template <int HD, int NCAP, int NS, int NQ>
+static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const KernelParams& kp, int grid, cudaStream_t stream) {
+    using C = Cfg<HD, NCAP, NS, NQ>;
+    auto kern = na3d_fwd_sm103<HD, NCAP, NS, NQ>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, C::SMEM_ALLOC, stream>>>(tq, tk, tv, kp);
+    return cudaGetLastError();
+}
+
+template <int HD, int NCAP, int NS, int NQ>
+static void info_t(VariantInfo* v) {
+    using C = Cfg<HD, NCAP, NS, NQ>;
+    v->ncap = NCAP;
+    v->stages = NS;
+    v->hd_box = C::HDB;
+    v->smem = C::SMEM_ALLOC;
+}
+
+// The instance table: (HD, score-tile cap, K/V stages, Q buffers).
+#define NA3D_VARIANTS(X) \
+    X(16, 128, 4, 2)     \
+    X(32, 128, 4, 2)     \
+    X(64, 128, 3, 2)     \
+    X(128, 128, 2, 1)    \
+    X(256, 64, 2, 1)
+
+bool variant_info(int hd, VariantInfo* info) {
+    switch (hd) {
+#define X(hd_, n_, s_, q_) \
+    case hd_:              \
+        info_t<hd_, n_, s_, q_>(info); \
+        return true;
+        NA3D_VARIANTS(X)
+#undef X
+        default:
+            return false;
+    }
+}
+
+cudaError_t launch_fwd(int hd, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const KernelParams& kp, int grid, cudaStream_t stream) {
+    switch (hd) {
+#define X(hd_, n_, s_, q_) \
+    case hd_:              \
+        return launch_t<hd_, n_, s_, q_>(tq, tk, tv, kp, grid, stream);
+        NA3D_VARIANTS(X)
+#undef X
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* flag) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(flag, g_na3d_timeout_flag, sizeof(unsigned int));
+    if (e != cudaSuccess) return e;
+    if (*flag) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_na3d_timeout_flag, &zero, sizeof(unsigned int));
+    }
+    return e;
+}
+
+}  // namespace na3d

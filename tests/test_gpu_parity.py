@@ -1,0 +1,201 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Bar: relative L2 error <= 5e-3 and max abs error <= 3e-2 against the
+unrounded fp64 oracle, on the same seeded inputs. Small and medium shapes are
+compared element by element over the whole output; the full benchmark shapes
+are compared on sampled rows (random rows plus every grid corner and edge
+row), which the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import na3d_inputs
+import neighborhood_attention_video_gb300 as na
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+REL_L2_MAX = 5e-3
+MAX_ABS_MAX = 3e-2
+
+
+def to_dev(a):
+    return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def from_dev(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run_gpu(q, k, v, kernel, stream=None):
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    out = torch.empty_like(qd)
+    na.na3d_fwd(qd, kd, vd, out, kernel, stream=stream)
+    torch.cuda.synchronize()
+    assert na.na3d_device_status() == 0
+    return from_dev(out)
+
+
+def errors(got_bits, want):
+    got = na3d_inputs.bf16_bits_to_f64(got_bits)
+    assert np.isfinite(got).all()
+    rel = float(np.linalg.norm((got - want).ravel()) / np.linalg.norm(want.ravel()))
+    mabs = float(np.abs(got - want).max())
+    return rel, mabs
+
+
+def check(got_bits, want, label):
+    rel, mabs = errors(got_bits, want)
+    print(f"{label}: rel_l2 {rel:.3e} max_abs {mabs:.3e}")
+    assert rel <= REL_L2_MAX, (label, rel)
+    assert mabs <= MAX_ABS_MAX, (label, mabs)
+
+
+# ------------------------------------------------------------ whole-output parity
+
+FULL_CASES = [
+    # (B, T, H, W, NH, HD), kernel          what it covers
+    ((1, 4, 8, 16, 2, 32), (3, 5, 5)),       # the tiny benchmark configuration, seed 0
+    ((1, 6, 20, 36, 2, 64), (3, 7, 7)),      # several bricks, ragged tails on every axis
+    ((2, 5, 13, 19, 3, 128), (3, 5, 7)),     # HD 128, B and NH > 1, ragged
+    ((1, 4, 9, 40, 2, 256), (3, 3, 11)),     # HD 256 (64-key chunks)
+    ((1, 3, 7, 11, 2, 16), (3, 5, 5)),       # HD 16
+    ((1, 16, 64, 5, 8, 64), (3, 5, 5)),      # narrow edge tile: W = KW = 5
+    ((1, 8, 24, 33, 2, 64), (3, 7, 33)),     # W = KW = 33
+    ((1, 16, 20, 20, 2, 64), (11, 11, 11)),  # large window
+    ((1, 3, 4, 150, 1, 64), (1, 3, 141)),    # W halo wider than one chunk: split W segments
+    ((1, 1, 12, 20, 2, 32), (1, 5, 7)),      # one frame (2-D)
+    ((1, 40, 1, 1, 2, 32), (7, 1, 1)),       # 1-D along T
+    ((1, 3, 5, 7, 2, 64), (3, 5, 7)),        # window = whole grid: full attention
+    ((1, 16, 64, 64, 8, 64), (3, 7, 7)),     # benchmark shape, (3,7,7)
+    ((1, 16, 64, 96, 8, 64), (3, 5, 5)),     # benchmark shape, (3,5,5)
+]
+
+
+@pytest.mark.parametrize("shape,kernel", FULL_CASES, ids=lambda x: "x".join(map(str, x)))
+def test_parity_whole_output(shape, kernel):
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=0)
+    got = run_gpu(q, k, v, kernel)
+    want = oracle.na3d_fwd(q, k, v, kernel)
+    check(got, want, f"{shape} {kernel}")
+
+
+# ------------------------------------------------------------ full sizes, sampled rows
+
+def sample_rows(shape, n_random, seed=0):
+    B, T, H, W, NH, HD = shape
+    rng = np.random.default_rng(seed)
+    rows = set(rng.integers(0, B * T * H * W * NH, size=n_random).tolist())
+    # corners and edge lines of the grid, for every batch and a few heads
+    for b in {0, B - 1}:
+        for n in {0, NH - 1}:
+            for t in {0, 1, T // 2, T - 2, T - 1}:
+                for h in {0, 1, H // 2, H - 2, H - 1}:
+                    for w in range(W):
+                        if t in (0, T - 1) or h in (0, H - 1) or w in (0, 1, W - 2, W - 1):
+                            tt, hh = min(max(t, 0), T - 1), min(max(h, 0), H - 1)
+                            rows.add(((((b * T + tt) * H + hh) * W + w) * NH) + n)
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+BIG_CASES = [
+    ((1, 16, 48, 48, 8, 64), (11, 11, 11)),
+    ((2, 16, 96, 128, 16, 128), (3, 7, 7)),
+    ((2, 8, 64, 33, 8, 64), (3, 7, 33)),
+]
+
+
+@pytest.mark.parametrize("shape,kernel", BIG_CASES, ids=lambda x: "x".join(map(str, x)))
+def test_parity_full_size_sampled(shape, kernel):
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=0)
+    got = run_gpu(q, k, v, kernel).reshape(-1, shape[-1])
+    rows = sample_rows(shape, 20000)
+    want = oracle.na3d_fwd_rows(q, k, v, kernel, rows)
+    check(got[rows], want, f"{shape} {kernel} ({rows.size} sampled rows)")
+
+
+# ------------------------------------------------------------ exact special cases
+
+def test_unit_window_returns_v_bit_exactly():
+    shape = (2, 5, 9, 13, 3, 64)
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=4)
+    got = run_gpu(q, k, v, (1, 1, 1))
+    np.testing.assert_array_equal(got, v)
+
+
+def test_constant_v_returns_the_constant():
+    shape = (1, 6, 17, 23, 2, 64)
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=9)
+    c = na3d_inputs.f64_to_bf16_bits(np.array([0.75]))[0]
+    v[...] = c
+    got = na3d_inputs.bf16_bits_to_f64(run_gpu(q, k, v, (3, 5, 7)))
+    # within one bf16 ulp of 0.75 (2^-8)
+    assert np.abs(got - 0.75).max() <= 2.0 ** -8
+    print("constant-V exact fraction:", float(np.mean(got == 0.75)))
+
+
+def test_axis_flip_equivariance():
+    shape = (1, 7, 12, 18, 2, 64)
+    kernel = (3, 5, 7)
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=21)
+    base = na3d_inputs.bf16_bits_to_f64(run_gpu(q, k, v, kernel))
+    for axis in (1, 2, 3):
+        fl = [np.ascontiguousarray(np.flip(x, axis=axis)) for x in (q, k, v)]
+        got = na3d_inputs.bf16_bits_to_f64(run_gpu(*fl, kernel))
+        ref = np.flip(base, axis=axis)
+        rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+        assert rel < 5e-3, (axis, rel)
+
+
+# ------------------------------------------------------------ launch behaviour
+
+def test_deterministic_and_stream_independent():
+    shape, kernel = (1, 6, 20, 36, 2, 64), (3, 7, 7)
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=3)
+    a = run_gpu(q, k, v, kernel)
+    b = run_gpu(q, k, v, kernel)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        c = run_gpu(q, k, v, kernel, stream=s)
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(a, c)
+
+
+def test_invalid_device_arguments_are_rejected():
+    shape = (1, 4, 8, 16, 2, 32)
+    x = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(x)
+    with pytest.raises(na.NA3DError) as e:
+        na.na3d_fwd(x, x, x, out, (4, 5, 5))
+    assert e.value.status == 3
+    with pytest.raises(na.NA3DError) as e:
+        na.na3d_fwd(x, x, x, x, (3, 5, 5))
+    assert e.value.status == 6
+    # a view starting 2 bytes into a buffer is not 16-byte aligned
+    flat = torch.zeros(x.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    mis = flat[1:1 + x.numel()].view(shape)
+    with pytest.raises(na.NA3DError) as e:
+        na.na3d_fwd(mis, x, x, out, (3, 5, 5))
+    assert e.value.status == 5
+
+
+def test_empty_batch_is_a_no_op():
+    x = torch.zeros((0, 4, 8, 16, 2, 32), dtype=torch.bfloat16, device="cuda")
+    na.na3d_fwd(x, x, x, torch.empty_like(x), (3, 5, 5))
+    torch.cuda.synchronize()
+
+
+def test_output_untouched_outside_the_tensor():
+    """The kernel writes exactly the output tensor: guard bands around it keep
+    their sentinel values."""
+    shape, kernel = (1, 5, 11, 13, 3, 64), (3, 5, 5)
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=5)
+    n = int(np.prod(shape))
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[guard:guard + n].view(shape)
+    na.na3d_fwd(to_dev(q), to_dev(k), to_dev(v), out, kernel)
+    torch.cuda.synchronize()
+    assert bool((buf[:guard] == 7.0).all()) and bool((buf[guard + n:] == 7.0).all())
+    check(from_dev(out.contiguous()), oracle.na3d_fwd(q, k, v, kernel), "guarded")
