@@ -1,0 +1,498 @@
+#!/usr/bin/env python
+"""Benchmark of the NA3D forward pass on GB300 (one JSON line on stdout).
+
+A step is one na3d_fwd call over the whole workload: bf16 (B,T,H,W,NH,HD)
+q, k, v resident in HBM, output written to HBM. The headline workload is
+B=1, T=16, H=64, W=64, NH=8, HD=64 with a (3,7,7) window; the other
+benchmark shapes are reported under "configs".
+
+Metric: useful TFLOPS = 4*B*T*H*W*NH*HD*KT*KH*KW / kernel time, and its
+fraction of the GB300 roofline, where the roofline time is the slower of the
+dense-bf16 tensor peak and the four tensors' bf16 bytes at HBM bandwidth
+(measured peaks from MEASURED_PEAKS.json).
+
+Timing: CUDA events on the launching stream around each kernel, L2 flushed
+(a buffer of twice the L2 size is overwritten) between timed steps, a
+barrier and a device synchronize on both sides of the K timed steps, and the
+maximum over ranks. SM clocks are sampled with nvidia-smi during the timed
+steps.
+
+--impl reference times the CPU oracle (fp64, all host cores) on a bounded
+sample of the same workload: the deliberately slow baseline.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload on its
+own GPU; the path has no cross-GPU exchange ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NA3D fwd useful TFLOPS and % of GB300 bf16 tensor roofline per config"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+WORKLOADS = {
+    # name: ((B, T, H, W, NH, HD), (KT, KH, KW))
+    "na3d_b1_t4_h8_w16_nh2_hd32_k3x5x5": ((1, 4, 8, 16, 2, 32), (3, 5, 5)),
+    "na3d_b1_t16_h64_w64_nh8_hd64_k3x7x7": ((1, 16, 64, 64, 8, 64), (3, 7, 7)),
+    "na3d_b1_t16_h64_w96_nh8_hd64_k3x5x5": ((1, 16, 64, 96, 8, 64), (3, 5, 5)),
+    "na3d_b1_t16_h64_w5_nh8_hd64_k3x5x5": ((1, 16, 64, 5, 8, 64), (3, 5, 5)),
+    "na3d_b1_t16_h48_w48_nh8_hd64_k11x11x11": ((1, 16, 48, 48, 8, 64), (11, 11, 11)),
+    "na3d_b2_t16_h96_w128_nh16_hd128_k3x7x7": ((2, 16, 96, 128, 16, 128), (3, 7, 7)),
+    "na3d_b2_t8_h64_w33_nh8_hd64_k3x7x33": ((2, 8, 64, 33, 8, 64), (3, 7, 33)),
+}
+HEADLINE = "na3d_b1_t16_h64_w64_nh8_hd64_k3x7x7"
+
+
+def useful_flops(shape, kernel):
+    B, T, H, W, NH, HD = shape
+    return 4.0 * B * T * H * W * NH * HD * kernel[0] * kernel[1] * kernel[2]
+
+
+def min_bytes(shape):
+    n = 1
+    for d in shape:
+        n *= d
+    return 4.0 * n * 2  # q, k, v read once, out written once, bf16
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def roofline_terms(shape, kernel, seconds, peaks):
+    flops, nbytes = useful_flops(shape, kernel), min_bytes(shape)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if t_tc >= t_hbm else "hbm"
+    return {
+        "bound": bound,
+        "useful_tflops": flops / seconds / 1e12,
+        "roofline_frac": max(t_tc, t_hbm) / seconds,
+        "achieved_gbs": nbytes / seconds / 1e9,
+        "roofline_us": max(t_tc, t_hbm) * 1e6,
+    }
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "neighborhood_attention_video_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu_id)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.15)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+        pg = dist
+    if args.impl == "ours":
+        torch.cuda.set_device(local)
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def allreduce_max(pg, x):
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def gpu_uuid(local):
+    import torch
+    try:
+        u = torch.cuda.get_device_properties(local).uuid
+        return f"GPU-{u}"
+    except Exception:
+        return local
+
+
+def time_kernel(shape, kernel, q, k, v, out, steps, warmup, flush, stream):
+    """Per-step CUDA-event kernel times (s) with the L2 flushed between steps."""
+    import torch
+    import neighborhood_attention_video_gb300 as na
+    for _ in range(warmup):
+        na.na3d_fwd(q, k, v, out, kernel, stream=stream)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            na.na3d_fwd(q, k, v, out, kernel, stream=stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e-3 for a, b in evs]
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import na3d_inputs
+    import neighborhood_attention_video_gb300 as na
+
+    world, rank, local, pg = dist_setup(args)
+    peaks, peak_src = load_peaks()
+    shape, kernel = WORKLOADS[args.workload]
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+
+    # inputs: the seeded recipe, generated into pinned host memory, then resident in HBM
+    n = int(np.prod(shape))
+    host = [torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    na3d_inputs.fill_qkv_host(*(t.data_ptr() for t in host), shape, seed=args.seed)
+    q, k, v = (t.to(dev) for t in host)
+    out = torch.empty_like(q)
+    host_out = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+
+    # warm-up, then K timed steps bracketed by barrier + synchronize
+    for _ in range(args.warmup):
+        na.na3d_fwd(q, k, v, out, kernel, stream=stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(gpu_uuid(local))
+    clocks.start()
+    barrier(pg)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    per_step = time_kernel(shape, kernel, q, k, v, out, args.steps, 0, flush, stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    kernel_s = allreduce_max(pg, sum(per_step)) / args.steps
+    status = na.na3d_device_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {na.na3d_status_string(status)}")
+
+    flops = useful_flops(shape, kernel)
+    terms = roofline_terms(shape, kernel, kernel_s, peaks)
+    value = world * flops / kernel_s / 1e12
+    plan = na.na3d_plan(*shape[1:], *kernel)
+    executed = plan["chunks_per_slice"] * shape[0] * shape[4] * 128 * plan["n_mma"] * shape[5] * 4.0
+
+    # e2e: pinned host -> HBM copies of q, k, v, the kernel, HBM -> pinned host copy of out
+    e2e_steps = max(3, min(args.steps, 30))
+    torch.cuda.synchronize()
+    barrier(pg)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(e2e_steps)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            a.record(stream)
+            for dst, src in zip((q, k, v), host):
+                dst.copy_(src, non_blocking=True)
+            na.na3d_fwd(q, k, v, out, kernel, stream=stream)
+            host_out.copy_(out, non_blocking=True)
+            b.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    e2e_s = allreduce_max(pg, sum(a.elapsed_time(b) for a, b in ev) * 1e-3) / e2e_steps
+    _ = float(host_out.view(torch.int16)[0, 0, 0, 0, 0, 0].item())  # the read-back result
+
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": kernel_s * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: q,k,v iid N(0,1) rounded to bf16, q pre-scaled by HD^-0.5, seed %d" % args.seed,
+        "config": {
+            "workload": args.workload,
+            "shape_BTHWNH_HD": list(shape),
+            "kernel": list(kernel),
+            "l2": "flushed between timed steps (2x L2 buffer overwritten)",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "plan": {k2: plan[k2] for k2 in ("bt", "bh", "bw", "cw", "cr", "n_mma")},
+        },
+        "roofline": {
+            "bound": terms["bound"],
+            "achieved": terms["achieved_gbs"] if terms["bound"] == "hbm" else terms["useful_tflops"],
+            "peak": peaks["hbm_gbs"] if terms["bound"] == "hbm" else peaks["bf16_tflops"],
+            "unit": "GB/s" if terms["bound"] == "hbm" else "TFLOP/s",
+            "frac": terms["roofline_frac"],
+            "peak_source": peak_src,
+            "traffic": ncu_traffic(args.workload),
+            "algorithmic_bytes": min_bytes(shape),
+            "useful_flops": flops,
+            "executed_mma_flops": executed,
+            "executed_tflops": executed / kernel_s / 1e12,
+            "kernel_us": kernel_s * 1e6,
+            "roofline_us": terms["roofline_us"],
+        },
+        "e2e": {
+            "value": world * flops / e2e_s / 1e12,
+            "unit": "TFLOPS",
+            "h2d_bytes_per_step": 3 * n * 2,
+            "d2h_bytes_per_step": n * 2,
+            "ms_per_step": e2e_s * 1e3,
+            "steps": e2e_steps,
+        },
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "timed_wall_s": wall,
+    }
+
+    if rank == 0 and not args.no_configs:
+        result["configs"] = per_config_table(dev, stream, flush, peaks)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(shape, kernel, args.seed, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def per_config_table(dev, stream, flush, peaks, steps=20, warmup=3):
+    """Every benchmark shape: useful TFLOPS and roofline fraction (seeded
+    torch N(0,1) inputs generated on the device; timing only)."""
+    import torch
+    import neighborhood_attention_video_gb300 as na
+    table = {}
+    gen = torch.Generator(device=dev)
+    for name, (shape, kernel) in WORKLOADS.items():
+        gen.manual_seed(0)
+        q = (torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+             * (1.0 / math.sqrt(shape[-1]))).to(torch.bfloat16)
+        k = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        v = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        times = time_kernel(shape, kernel, q, k, v, out, steps, warmup, flush, stream)
+        t = statistics.median(times)
+        terms = roofline_terms(shape, kernel, t, peaks)
+        plan = na.na3d_plan(*shape[1:], *kernel)
+        executed = plan["chunks_per_slice"] * shape[0] * shape[4] * 128 * plan["n_mma"] * shape[5] * 4.0
+        table[name] = {
+            "us": t * 1e6,
+            "useful_tflops": terms["useful_tflops"],
+            "roofline_frac": terms["roofline_frac"],
+            "bound": terms["bound"],
+            "roofline_us": terms["roofline_us"],
+            "executed_tflops": executed / t / 1e12,
+            "plan": [plan["bt"], plan["bh"], plan["bw"], plan["cw"], plan["cr"], plan["n_mma"]],
+        }
+        del q, k, v, out
+    torch.cuda.synchronize()
+    return table
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample_rate(shape, kernel, seed, budget_s, nthreads):
+    """Time the fp64 oracle on a random sample of output rows of the workload,
+    sized to take about `budget_s`; returns (useful TFLOPS, rows, seconds)."""
+    import numpy as np
+
+    import na3d_inputs
+    import oracle
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=seed)
+    total = int(np.prod(shape[:5]))
+    per_row = 4.0 * shape[5] * kernel[0] * kernel[1] * kernel[2]
+    rng = np.random.default_rng(seed)
+    n = min(total, 2048)
+    rows = rng.choice(total, size=n, replace=False)
+    t0 = time.perf_counter()
+    oracle.na3d_fwd_rows(q, k, v, kernel, rows, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    n2 = int(min(total, max(n, n * budget_s / max(dt, 1e-6))))
+    if n2 > n:
+        rows = rng.choice(total, size=n2, replace=False)
+        t0 = time.perf_counter()
+        oracle.na3d_fwd_rows(q, k, v, kernel, rows, nthreads=nthreads)
+        dt = time.perf_counter() - t0
+        n = n2
+    return per_row * n / dt / 1e12, n, dt
+
+
+def cpu_baseline(shape, kernel, seed, budget_s=10.0):
+    cores = os.cpu_count() or 1
+    tf, n, dt = oracle_sample_rate(shape, kernel, seed, budget_s, cores)
+    return {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+            "sample": f"{n} random output rows (b,t,h,w,head) of the workload, fp64 oracle, {dt:.1f} s"}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    world, rank, local, pg = dist_setup(args)
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+    import numpy as np
+
+    import na3d_inputs
+    import oracle
+    shape, kernel = WORKLOADS[args.workload]
+    cores = os.cpu_count() or 1
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=args.seed)
+    total = int(np.prod(shape[:5]))
+    per_row = 4.0 * shape[5] * kernel[0] * kernel[1] * kernel[2]
+    rng = np.random.default_rng(args.seed)
+    # size each step so the whole run stays within about args.cpu_seconds * 6
+    probe = rng.choice(total, size=min(total, 512), replace=False)
+    t0 = time.perf_counter()
+    oracle.na3d_fwd_rows(q, k, v, kernel, probe, nthreads=cores)
+    rate = probe.size / max(time.perf_counter() - t0, 1e-6)
+    budget = 6.0 * args.cpu_seconds
+    rows_per_step = int(max(64, min(total, rate * budget / (args.steps + args.warmup))))
+    for _ in range(args.warmup):
+        oracle.na3d_fwd_rows(q, k, v, kernel, rng.choice(total, size=rows_per_step), nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.na3d_fwd_rows(q, k, v, kernel, rng.choice(total, size=rows_per_step), nthreads=cores)
+    dt = time.perf_counter() - t0
+    value = per_row * rows_per_step * args.steps / dt / 1e12
+    res = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same recipe and seed)",
+        "config": {"workload": args.workload, "shape_BTHWNH_HD": list(shape), "kernel": list(kernel)},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_per_step} random output rows per step"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(res), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-configs", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -58,7 +58,8 @@ enum na3d_status {
  *   read only and may alias one another; out must not overlap any of them.
  * B: batch size, >= 0.  T, H, W: grid sizes, >= 1.  NH: heads, >= 0.
  *   B == 0 or NH == 0 is an empty problem: the call returns NA3D_OK after
- *   validation and enqueues nothing.
+ *   validating the sizes, enqueues nothing, and does not look at the
+ *   pointers (which may be NULL).
  * HD: head dimension, a power of two in [16, 256].
  * KT, KH, KW: odd window lengths with 1 <= KT <= T, 1 <= KH <= H, 1 <= KW <= W.
  * stream: a cudaStream_t on the current device (NULL = legacy default stream).

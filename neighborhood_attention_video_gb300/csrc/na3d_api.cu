@@ -221,14 +221,14 @@ int na3d_plan(int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t K
 int na3d_fwd(const void* q, const void* k, const void* v, void* out, int64_t B, int64_t T,
              int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT, int64_t KH, int64_t KW,
              void* stream) {
-    if (!q || !k || !v || !out) return NA3D_ERR_NULL;
     int rc = validate_shape(B, T, H, W, NH, HD, KT, KH, KW);
     if (rc != NA3D_OK) return rc;
+    const int64_t bytes = B * T * H * W * NH * HD * 2;
+    if (bytes == 0) return NA3D_OK;  // B == 0 or NH == 0: nothing to read or write
+    if (!q || !k || !v || !out) return NA3D_ERR_NULL;
     const void* ptrs[4] = {q, k, v, out};
     for (const void* p : ptrs)
         if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return NA3D_ERR_ALIGN;
-    const int64_t bytes = B * T * H * W * NH * HD * 2;
-    if (bytes == 0) return NA3D_OK;  // B == 0 or NH == 0: nothing to compute
     if (overlaps(out, q, bytes) || overlaps(out, k, bytes) || overlaps(out, v, bytes))
         return NA3D_ERR_ALIAS;
 

@@ -61,6 +61,7 @@ struct Cfg {
     static constexpr int P_REG = 128 * 128;         // 64 bf16 key columns x 128 rows
     static constexpr int P_TILE = (NCAP / 64) * P_REG;
     static constexpr int NW = NCAP / 32;            // 32-column words per score row
+    static constexpr int OPIECES = (HD + 31) / 32;  // 32-column TMEM loads per output row
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
     static constexpr int OFF_V = OFF_K + NS * KV_TILE;
@@ -78,7 +79,7 @@ struct Cfg {
     static constexpr uint32_t TM_S = 0;            // score buffers: [0, NCAP), [NCAP, 2 NCAP)
     static constexpr uint32_t TM_O = 2 * NCAP;     // output accumulator: HD columns
     static constexpr uint32_t TM_COLS = 512;
-    static_assert(TM_O + HD <= TM_COLS, "TMEM budget");
+    static_assert(TM_O + OPIECES * 32 <= TM_COLS, "TMEM budget");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(NCAP == 64 || NCAP == 128, "score tile width");
     static_assert(NS >= 2, "the K/V ring needs two stages to avoid a producer/MMA cycle");
@@ -411,7 +412,7 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
                 tc_fence_after();
                 const float a = rescale ? alpha : 1.f;
 #pragma unroll 1
-                for (int q = 0; q < C::HD / 32; ++q) {
+                for (int q = 0; q < C::OPIECES; ++q) {  // HD = 16 also scales 16 unused columns
                     float o[32];
                     tmem_ld32(t_row + C::TM_O + q * 32, o);
                     tmem_wait_ld();
@@ -432,7 +433,7 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
         const int64_t tok = ((static_cast<int64_t>(U.b) * p.T + t) * p.H + h) * p.W + w;
         uint16_t* orow = p.out + (tok * p.NH + U.n) * C::HD;
 #pragma unroll 1
-        for (int q = 0; q < C::HD / 32; ++q) {
+        for (int q = 0; q < C::OPIECES; ++q) {
             float o[32];
             tmem_ld32(t_row + C::TM_O + q * 32, o);
             tmem_wait_ld();
@@ -441,8 +442,9 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
             for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(o[2 * j] * inv, o[2 * j + 1] * inv);
             if (valid) {
                 uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
+                constexpr int kVec = (C::HD < 32 ? C::HD : 32) / 8;   // 16-byte stores per piece
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < kVec; ++i)
                     dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
             }
         }

@@ -86,6 +86,7 @@ def test_pointer_validation(lib):
 def test_empty_problem_is_a_no_op(lib):
     assert call_fwd(lib, (16, 32, 48, 64), dims=(0, 4, 8, 16, 2, 32)) == OK
     assert call_fwd(lib, (16, 32, 48, 64), dims=(1, 4, 8, 16, 0, 32)) == OK
+    assert call_fwd(lib, (0, 0, 0, 0), dims=(0, 4, 8, 16, 2, 32)) == OK  # empty tensors may be NULL
 
 
 def test_valid_call_without_gpu_fails_loudly(lib):
