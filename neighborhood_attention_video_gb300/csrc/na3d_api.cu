@@ -263,7 +263,8 @@ int na3d_fwd(const void* q, const void* k, const void* v, void* out, int64_t B, 
         !encode_map(&tv, v, B, T, H, W, NH, HD, vi.hd_box, pl.cw, pl.cr, 1))
         return NA3D_ERR_CUDA;
 
-    const int grid = int(units < sms ? units : sms);
+    const int64_t slots = int64_t(sms) * vi.ctas_per_sm;   // persistent CTAs
+    const int grid = int(units < slots ? units : slots);
     if (na3d::launch_fwd(int(HD), tq, tk, tv, kp, grid, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return NA3D_ERR_CUDA;

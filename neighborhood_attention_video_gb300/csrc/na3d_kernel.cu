@@ -14,15 +14,23 @@
 // one frame (t), loaded with one TMA box per 64 head-dim columns. Queries are
 // the M = 128 rows of every tensor-core tile; a chunk's keys are its N columns.
 //
-// Roles (192 threads, one CTA per SM, loop over units):
-//   warp 0      TMA producer: Q brick once per unit, K and V per chunk into a
-//               ring of `NS` stages.
-//   warp 1      tensor-core issuer: S = Q K^T into one of two TMEM score
-//               buffers, then O += P V into the TMEM output accumulator; owns
-//               the tensor-memory allocation.
-//   warps 2..5  softmax: one query row per thread (TMEM lane), window mask,
-//               running max / sum in log2 space, P as bf16 into shared memory,
-//               occasional O rescale, and the epilogue O / l -> bf16 -> HBM.
+// Roles (256 threads; two CTAs per SM for HD <= 128, one for HD = 256):
+//   warps 0..3  softmax (warpgroup 0): one query row per thread (its TMEM
+//               lane): window mask, running max and sum in log2 space, P as
+//               bf16 into tensor memory, occasional O rescale, and the
+//               epilogue O / l -> bf16 -> HBM.
+//   warp 4      TMA producer: the Q brick once per unit; K and V of each chunk
+//               into rings of NS stages with separate barriers, K one chunk
+//               ahead of V.
+//   warp 5      tensor-core issuer: S = Q K^T (A, B in shared memory) into the
+//               TMEM score tile, then O += P V with P read from tensor memory;
+//               owns the tensor-memory allocation.
+//   warps 6, 7  idle (they complete warpgroup 1 for the register hand-over).
+//
+// Tensor memory per CTA: S (NCAP fp32 columns), P (NCAP/2 columns of bf16
+// pairs) and O (HD columns). S is free again as soon as the softmax has read
+// it into registers, so the next score tile is computed while the softmax
+// works on the current one.
 //
 // Every pipeline wait is bounded: a wait that runs out sets a device flag, all
 // roles drop out of their loops, in-flight copies and MMAs are drained, and
@@ -39,16 +47,16 @@ __device__ unsigned int g_na3d_timeout_flag = 0;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 500000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
-// A new running maximum replaces the reference maximum only when it exceeds it
-// by more than this (log2 units): probabilities stay <= 2^8 and the O rescale
-// (a TMEM round trip) is rare.
+// The reference maximum (log2 units) is raised only when a chunk's maximum
+// exceeds it by more than this, so probabilities stay <= 2^8 and the O
+// rescale (a TMEM round trip) is rare.
 constexpr float kRescaleThreshold = 8.0f;
-constexpr int kThreads = 192;
-constexpr int kMinSmem = 120 * 1024;  // forces one CTA per SM (each CTA takes all 512 TMEM columns)
+constexpr uint32_t kBf16Limit = 0x4380u;   // bf16 bit pattern of 2^8
+constexpr int kThreads = 256;
 
-template <int HD_, int NCAP_, int NS_, int NQ_>
+template <int HD_, int NCAP_, int NS_, int NQ_, int CPS_>
 struct Cfg {
-    static constexpr int HD = HD_, NCAP = NCAP_, NS = NS_, NQ = NQ_;
+    static constexpr int HD = HD_, NCAP = NCAP_, NS = NS_, NQ = NQ_, CPS = CPS_;
     static constexpr int HDB = HD < 64 ? HD : 64;   // head-dim columns per TMA box / smem row
     static constexpr int NREG = HD / HDB;           // boxes (smem regions) per tile
     static constexpr int ROWB = HDB * 2;            // bytes per smem row
@@ -58,31 +66,38 @@ struct Cfg {
     static constexpr int Q_TILE = NREG * Q_REG;
     static constexpr int KV_REG = NCAP * ROWB;
     static constexpr int KV_TILE = NREG * KV_REG;
-    static constexpr int P_REG = 128 * 128;         // 64 bf16 key columns x 128 rows
-    static constexpr int P_TILE = (NCAP / 64) * P_REG;
     static constexpr int NW = NCAP / 32;            // 32-column words per score row
     static constexpr int OPIECES = (HD + 31) / 32;  // 32-column TMEM loads per output row
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
     static constexpr int OFF_V = OFF_K + NS * KV_TILE;
-    static constexpr int OFF_P = OFF_V + NS * KV_TILE;
-    static constexpr int OFF_BAR = OFF_P + 2 * P_TILE;
+    static constexpr int OFF_BAR = OFF_V + NS * KV_TILE;
     // barrier indices
-    static constexpr int B_QFULL = 0, B_QEMPTY = NQ, B_KVFULL = 2 * NQ, B_KVEMPTY = 2 * NQ + NS;
-    static constexpr int B_SFULL = 2 * NQ + 2 * NS, B_SEMPTY = B_SFULL + 2, B_PFULL = B_SFULL + 4,
-                         B_PVDONE = B_SFULL + 6, B_OFULL = B_SFULL + 8, B_OEMPTY = B_SFULL + 9,
-                         B_DRAIN = B_SFULL + 10, NBAR = B_SFULL + 11;
+    static constexpr int B_QFULL = 0, B_QEMPTY = NQ;
+    static constexpr int B_KFULL = 2 * NQ, B_KEMPTY = B_KFULL + NS;
+    static constexpr int B_VFULL = B_KEMPTY + NS, B_VEMPTY = B_VFULL + NS;
+    static constexpr int B_SFULL = B_VEMPTY + NS, B_SEMPTY = B_SFULL + 1, B_PFULL = B_SFULL + 2,
+                         B_PVDONE = B_SFULL + 3, B_OFULL = B_SFULL + 4, B_OEMPTY = B_SFULL + 5,
+                         B_DRAIN = B_SFULL + 6, NBAR = B_SFULL + 7;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
-    static constexpr int SMEM_ALLOC =
-        (SMEM_USED + 1024) > kMinSmem ? (SMEM_USED + 1024) : kMinSmem;
-    static constexpr uint32_t TM_S = 0;            // score buffers: [0, NCAP), [NCAP, 2 NCAP)
-    static constexpr uint32_t TM_O = 2 * NCAP;     // output accumulator: HD columns
-    static constexpr uint32_t TM_COLS = 512;
-    static_assert(TM_O + OPIECES * 32 <= TM_COLS, "TMEM budget");
-    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    // The floor keeps the CTA count per SM at CPS (tensor memory is sized for it).
+    static constexpr int MIN_SMEM = CPS == 2 ? 80 * 1024 : 120 * 1024;
+    static constexpr int SMEM_ALLOC = (SMEM_USED + 1024) > MIN_SMEM ? (SMEM_USED + 1024) : MIN_SMEM;
+    static constexpr uint32_t TM_S = 0;                    // NCAP fp32 score columns
+    static constexpr uint32_t TM_P = NCAP;                 // NCAP / 2 columns of bf16 pairs
+    static constexpr uint32_t TM_O = NCAP + NCAP / 2;      // HD fp32 output columns
+    static constexpr uint32_t TM_NEED = TM_O + OPIECES * 32;
+    static constexpr uint32_t TM_COLS = TM_NEED <= 256 ? 256 : 512;
+    // registers: warpgroup 1 gives its share to the softmax warpgroup
+    static constexpr uint32_t REGS_LAUNCH = 65536 / (kThreads * CPS) >= 256 ? 255 : 65536 / (kThreads * CPS);
+    static constexpr uint32_t REGS_LOW = 56;
+    static constexpr uint32_t REGS_HIGH = CPS == 2 ? 200 : 232;
+    static_assert(CPS == 1 || (REGS_HIGH + REGS_LOW) * 128 <= REGS_LAUNCH * kThreads, "register split");
+    static_assert(TM_COLS * CPS <= 512, "TMEM budget");
+    static_assert(SMEM_ALLOC * CPS <= 232448, "shared memory budget");
     static_assert(NCAP == 64 || NCAP == 128, "score tile width");
-    static_assert(NS >= 2, "the K/V ring needs two stages to avoid a producer/MMA cycle");
+    static_assert(NS >= 2, "K/V rings need two stages");
 };
 
 // ------------------------------------------------------------------ geometry
@@ -172,34 +187,53 @@ struct Sync {
     }
 };
 
-// ------------------------------------------------------------------ roles
+// ------------------------------------------------------------------ producer
+
+struct ChunkCoords {
+    int x, kw0, kh0, kt, b;
+};
 
 template <class C>
 __device__ void producer_role(const KernelParams& p, const CUtensorMap* tq, const CUtensorMap* tk,
                               const CUtensorMap* tv, const Sync& sy, uint32_t base) {
-    uint32_t g = 0, ul = 0, nq = 0;
+    uint32_t gk = 0, gv = 0, nq = 0;   // K chunks, V chunks and Q bricks issued
+    ChunkCoords prev{0, 0, 0, 0, 0};
+    const uint32_t kv_bytes = C::NREG * C::ROWB * p.cw * p.cr;
+
+    auto load_v = [&](const ChunkCoords& cc) -> bool {
+        const uint32_t st = gv % C::NS;
+        if (!sy.wait(sy.bar(C::B_VEMPTY + st), ((gv / C::NS) & 1u) ^ 1u)) return false;
+        const uint32_t full = sy.bar(C::B_VFULL + st);
+        mbar_arrive_expect_tx(full, kv_bytes);
+#pragma unroll
+        for (int r = 0; r < C::NREG; ++r)
+            tma_load_5d(base + C::OFF_V + st * C::KV_TILE + r * C::KV_REG, tv, full,
+                        cc.x + r * C::HDB, cc.kw0, cc.kh0, cc.kt, cc.b);
+        ++gv;
+        return true;
+    };
+
     bool ok = true;
+    uint32_t ul = 0;
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++ul) {
         const Unit U = unit_of(p, u);
         const int xq = U.n * C::HD;
         ChunkCursor cur{U.lo_t, 0, 0};
-        for (int c = 0; c < U.nch; ++c, ++g) {
-            const uint32_t st = g % C::NS;
-            if (!sy.wait(sy.bar(C::B_KVEMPTY + st), ((g / C::NS) & 1u) ^ 1u)) { ok = false; break; }
-            const uint32_t full = sy.bar(C::B_KVFULL + st);
-            mbar_arrive_expect_tx(full, 2u * C::NREG * C::ROWB * p.cw * p.cr);
-            const int kh0 = U.lo_h + cur.hc * p.cr, kw0 = U.lo_w + cur.wc * p.cw;
-#pragma unroll
-            for (int r = 0; r < C::NREG; ++r) {
-                tma_load_5d(base + C::OFF_K + st * C::KV_TILE + r * C::KV_REG, tk, full,
-                            xq + r * C::HDB, kw0, kh0, cur.kt, U.b);
-                tma_load_5d(base + C::OFF_V + st * C::KV_TILE + r * C::KV_REG, tv, full,
-                            xq + r * C::HDB, kw0, kh0, cur.kt, U.b);
-            }
+        for (int c = 0; c < U.nch; ++c) {
+            const ChunkCoords cc{xq, U.lo_w + cur.wc * p.cw, U.lo_h + cur.hc * p.cr, cur.kt, U.b};
             cur.advance(U);
-            if (c == 0) {  // the Q brick goes right behind the unit's first K/V chunk
+            const uint32_t st = gk % C::NS;
+            if (!sy.wait(sy.bar(C::B_KEMPTY + st), ((gk / C::NS) & 1u) ^ 1u)) { ok = false; break; }
+            const uint32_t full = sy.bar(C::B_KFULL + st);
+            mbar_arrive_expect_tx(full, kv_bytes);
+#pragma unroll
+            for (int r = 0; r < C::NREG; ++r)
+                tma_load_5d(base + C::OFF_K + st * C::KV_TILE + r * C::KV_REG, tk, full,
+                            cc.x + r * C::HDB, cc.kw0, cc.kh0, cc.kt, cc.b);
+            ++gk;
+            if (c == 0) {  // the Q brick goes right behind the unit's first K chunk
                 const uint32_t qb = ul % C::NQ;
-                if (!sy.wait(sy.bar(C::B_QEMPTY + qb), ((ul / C::NQ) & 1u) ^ 1u)) { ok = false; ++g; break; }
+                if (!sy.wait(sy.bar(C::B_QEMPTY + qb), ((ul / C::NQ) & 1u) ^ 1u)) { ok = false; break; }
                 const uint32_t qf = sy.bar(C::B_QFULL + qb);
                 mbar_arrive_expect_tx(qf, C::NREG * C::ROWB * p.bt * p.bh * p.bw);
 #pragma unroll
@@ -208,18 +242,25 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tq, cons
                                 xq + r * C::HDB, U.w0, U.h0, U.t0, U.b);
                 ++nq;
             }
+            if (gk >= 2 && !load_v(prev)) { ok = false; break; }   // V trails K by one chunk
+            prev = cc;
         }
     }
+    if (ok && gk > gv) load_v(prev);
     // Drain: every issued load must land before the CTA may exit.
     for (uint32_t s = 0; s < C::NS; ++s) {
-        const uint32_t fills = g / C::NS + (s < g % C::NS ? 1u : 0u);
-        if (fills) mbar_wait_bounded(sy.bar(C::B_KVFULL + s), (fills - 1u) & 1u, kDrainLimitNs);
+        const uint32_t fk = gk / C::NS + (s < gk % C::NS ? 1u : 0u);
+        if (fk) mbar_wait_bounded(sy.bar(C::B_KFULL + s), (fk - 1u) & 1u, kDrainLimitNs);
+        const uint32_t fv = gv / C::NS + (s < gv % C::NS ? 1u : 0u);
+        if (fv) mbar_wait_bounded(sy.bar(C::B_VFULL + s), (fv - 1u) & 1u, kDrainLimitNs);
     }
     for (uint32_t s = 0; s < C::NQ; ++s) {
-        const uint32_t fills = nq / C::NQ + (s < nq % C::NQ ? 1u : 0u);
-        if (fills) mbar_wait_bounded(sy.bar(C::B_QFULL + s), (fills - 1u) & 1u, kDrainLimitNs);
+        const uint32_t fq = nq / C::NQ + (s < nq % C::NQ ? 1u : 0u);
+        if (fq) mbar_wait_bounded(sy.bar(C::B_QFULL + s), (fq - 1u) & 1u, kDrainLimitNs);
     }
 }
+
+// ------------------------------------------------------------------ tensor-core issuer
 
 template <class C>
 __device__ void mma_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem) {
@@ -227,23 +268,23 @@ __device__ void mma_role(const KernelParams& p, const Sync& sy, uint32_t base, u
     const uint32_t idesc_o = make_idesc_bf16(128, C::HD, 0, 1);
     uint32_t g = 0, ul = 0;
 
-    // O += P_g V_g; `first` marks the unit's first product (overwrites O).
+    // O += P_g V_g with P in tensor memory; `first` marks the unit's first
+    // product (it overwrites O).
     auto issue_pv = [&](uint32_t gp, bool first) -> bool {
-        const uint32_t sb = gp & 1u, st = gp % C::NS;
+        const uint32_t st = gp % C::NS;
         if (first && !sy.wait(sy.bar(C::B_OEMPTY), (ul & 1u) ^ 1u)) return false;
-        if (!sy.wait(sy.bar(C::B_PFULL + sb), (gp >> 1) & 1u)) return false;
+        if (!sy.wait(sy.bar(C::B_VFULL + st), (gp / C::NS) & 1u)) return false;
+        if (!sy.wait(sy.bar(C::B_PFULL), gp & 1u)) return false;
         tc_fence_after();
-        const uint32_t pa = base + C::OFF_P + sb * C::P_TILE;
         const uint32_t va = base + C::OFF_V + st * C::KV_TILE;
         const int ksteps = p.n_mma >> 4;
         for (int kk = 0; kk < ksteps; ++kk) {
-            const uint64_t ad = make_smem_desc(pa + (kk >> 2) * C::P_REG + (kk & 3) * 32, 16, 1024,
-                                               kSwizzle128B);
             const uint64_t bd = make_smem_desc(va + kk * 16 * C::ROWB, C::KV_REG, C::SBO, C::SWZ);
-            umma_bf16_ss(tmem + C::TM_O, ad, bd, idesc_o, (first && kk == 0) ? 0u : 1u);
+            umma_bf16_ts(tmem + C::TM_O, tmem + C::TM_P + kk * 8, bd, idesc_o,
+                         (first && kk == 0) ? 0u : 1u);
         }
-        umma_commit(sy.bar(C::B_PVDONE + sb));
-        umma_commit(sy.bar(C::B_KVEMPTY + st));
+        umma_commit(sy.bar(C::B_PVDONE));
+        umma_commit(sy.bar(C::B_VEMPTY + st));
         return true;
     };
 
@@ -252,12 +293,11 @@ __device__ void mma_role(const KernelParams& p, const Sync& sy, uint32_t base, u
         const Unit U = unit_of(p, u);
         const uint32_t qb = ul % C::NQ;
         if (!sy.wait(sy.bar(C::B_QFULL + qb), (ul / C::NQ) & 1u)) break;
-        tc_fence_after();
         const uint32_t qa = base + C::OFF_Q + qb * C::Q_TILE;
         for (int c = 0; c < U.nch; ++c, ++g) {
-            const uint32_t st = g % C::NS, sb = g & 1u;
-            if (!sy.wait(sy.bar(C::B_KVFULL + st), (g / C::NS) & 1u)) { ok = false; break; }
-            if (!sy.wait(sy.bar(C::B_SEMPTY + sb), ((g >> 1) & 1u) ^ 1u)) { ok = false; break; }
+            const uint32_t st = g % C::NS;
+            if (!sy.wait(sy.bar(C::B_KFULL + st), (g / C::NS) & 1u)) { ok = false; break; }
+            if (!sy.wait(sy.bar(C::B_SEMPTY), (g & 1u) ^ 1u)) { ok = false; break; }
             tc_fence_after();
             const uint32_t ka = base + C::OFF_K + st * C::KV_TILE;
 #pragma unroll
@@ -265,9 +305,10 @@ __device__ void mma_role(const KernelParams& p, const Sync& sy, uint32_t base, u
                 const int reg = kk / (C::HDB / 16), sub = kk % (C::HDB / 16);
                 const uint64_t ad = make_smem_desc(qa + reg * C::Q_REG + sub * 32, 16, C::SBO, C::SWZ);
                 const uint64_t bd = make_smem_desc(ka + reg * C::KV_REG + sub * 32, 16, C::SBO, C::SWZ);
-                umma_bf16_ss(tmem + C::TM_S + sb * C::NCAP, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                umma_bf16_ss(tmem + C::TM_S, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
             }
-            umma_commit(sy.bar(C::B_SFULL + sb));
+            umma_commit(sy.bar(C::B_SFULL));
+            umma_commit(sy.bar(C::B_KEMPTY + st));
             if (c == U.nch - 1) umma_commit(sy.bar(C::B_QEMPTY + qb));
             if (c > 0 && !issue_pv(g - 1, c == 1)) { ok = false; break; }
         }
@@ -280,15 +321,58 @@ __device__ void mma_role(const KernelParams& p, const Sync& sy, uint32_t base, u
     mbar_wait_bounded(sy.bar(C::B_DRAIN), 0, kDrainLimitNs);
 }
 
+// ------------------------------------------------------------------ softmax
+
+// P = 2^(s log2e - moff) for the masked score row (masked keys give 0), as
+// bf16 pairs into tensor memory; returns the fp32 sum of the probabilities and
+// folds the bf16 maximum into *pmax.
 template <class C>
-__device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem,
-                             int warp, int lane) {
-    const int quarter = warp & 3;               // TMEM lanes this warp may access
-    const int r = quarter * 32 + lane;          // tile row = query of the brick
-    const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+__device__ __forceinline__ float write_probabilities(const float* s, const uint32_t* m,
+                                                     const bool* live, int n_mma, float moff,
+                                                     uint32_t p_addr, uint32_t* pmax) {
+    const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
+    const uint64_t neg2 = f2_pack(-moff, -moff);
+    uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+    uint32_t mx = 0u;
+#pragma unroll
+    for (int q = 0; q < C::NW; ++q) {
+        if (q * 32 < n_mma) {
+            uint32_t pk[16];
+            if (live[q]) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float x0 = ((m[q] >> (2 * j)) & 1u) ? s[32 * q + 2 * j] : -INFINITY;
+                    const float x1 = ((m[q] >> (2 * j + 1)) & 1u) ? s[32 * q + 2 * j + 1] : -INFINITY;
+                    float e0, e1;
+                    f2_unpack(f2_fma(f2_pack(x0, x1), l2e2, neg2), e0, e1);
+                    e0 = ex2_approx(e0);
+                    e1 = ex2_approx(e1);
+                    pk[j] = pack_bf16x2(e0, e1);
+                    mx = bf16x2_max(mx, pk[j]);
+                    if (j & 1) acc1 = f2_add(acc1, f2_pack(e0, e1));
+                    else acc0 = f2_add(acc0, f2_pack(e0, e1));
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) pk[j] = 0u;
+            }
+            tmem_st16(p_addr + q * 16, pk);
+        }
+    }
+    *pmax = mx;
+    float a0, a1, b0, b1;
+    f2_unpack(acc0, a0, a1);
+    f2_unpack(acc1, b0, b1);
+    return (a0 + a1) + (b0 + b1);
+}
+
+template <class C>
+__device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t tmem, int warp,
+                             int lane) {
+    const int r = warp * 32 + lane;             // tile row = query of the brick = TMEM lane
+    const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const int M = p.bt * p.bh * p.bw;
     const int iw = r % p.bw, ih = (r / p.bw) % p.bh, it = r / (p.bw * p.bh);
-    const uint32_t p_row_off = (r >> 3) * 1024 + (r & 7) * 128;
     uint32_t g = 0, ul = 0;
 
     for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++ul) {
@@ -310,20 +394,19 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
             }
         }
         float m_ref = -INFINITY;   // reference maximum, log2 units
-        float l = 0.f;             // running sum of the bf16-rounded probabilities
+        float l = 0.f;             // running sum of the probabilities
         ChunkCursor cur{U.lo_t, 0, 0};
 
         for (int c = 0; c < U.nch; ++c, ++g) {
-            const uint32_t sb = g & 1u;
-            if (!sy.wait(sy.bar(C::B_SFULL + sb), (g >> 1) & 1u)) return;
+            if (!sy.wait(sy.bar(C::B_SFULL), g & 1u)) return;
             tc_fence_after();
             float s[C::NCAP];
 #pragma unroll
             for (int q = 0; q < C::NW; ++q)
-                if (q * 32 < p.n_mma) tmem_ld32(t_row + C::TM_S + sb * C::NCAP + q * 32, s + 32 * q);
+                if (q * 32 < p.n_mma) tmem_ld32(t_row + C::TM_S + q * 32, s + 32 * q);
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(sy.bar(C::B_SEMPTY + sb));
+            mbar_arrive(sy.bar(C::B_SEMPTY));   // the next score tile may overwrite S now
 
             // window mask of this row over the chunk's cr x cw keys
             uint32_t m[4] = {0u, 0u, 0u, 0u};
@@ -342,74 +425,59 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
                 }
             }
             cur.advance(U);
-
             bool live[C::NW];
-            float mx = -INFINITY;
 #pragma unroll
-            for (int q = 0; q < C::NW; ++q) {
+            for (int q = 0; q < C::NW; ++q)
                 live[q] = (q * 32 < p.n_mma) && __any_sync(0xffffffffu, m[q] != 0u);
-                if (live[q]) {
-#pragma unroll
-                    for (int b = 0; b < 32; ++b) {
-                        const float x = ((m[q] >> b) & 1u) ? s[32 * q + b] : -INFINITY;
-                        s[32 * q + b] = x;
-                        mx = fmaxf(mx, x);
-                    }
-                }
+            const bool has_keys = (m[0] | m[1] | m[2] | m[3]) != 0u;
+
+            // P and O are free once the previous product has completed.
+            if (!sy.wait(sy.bar(C::B_PVDONE), (g & 1u) ^ 1u)) return;
+            tc_fence_after();
+
+            // Fast path: keep the reference maximum and check afterwards that
+            // no probability exceeded 2^8. Rows meeting their first keys, or a
+            // maximum that grew by more than 2^8, take the exact path.
+            bool slow = __any_sync(0xffffffffu, has_keys && m_ref == -INFINITY);
+            float lsum = 0.f;
+            if (!slow) {
+                uint32_t pmax;
+                lsum = write_probabilities<C>(s, m, live, p.n_mma, m_ref == -INFINITY ? 0.f : m_ref,
+                                              t_row + C::TM_P, &pmax);
+                const uint32_t top = max(pmax >> 16, pmax & 0xffffu);
+                slow = __any_sync(0xffffffffu, top > kBf16Limit);
+                if (slow) tmem_wait_st();
             }
-            const float mx2 = mx * kLog2e;
             float alpha = 1.f;
             bool rescale = false;
-            if (mx2 > m_ref + kRescaleThreshold) {
-                if (m_ref != -INFINITY) {
-                    alpha = ex2_approx(m_ref - mx2);
-                    rescale = true;
-                }
-                m_ref = mx2;
-            }
-            const float moff = m_ref == -INFINITY ? 0.f : m_ref;
-            l *= alpha;
-
-            // P buffer `sb` is free once the product two chunks back is done.
-            if (!sy.wait(sy.bar(C::B_PVDONE + sb), ((g >> 1) & 1u) ^ 1u)) return;
-            const uint32_t prow = base + C::OFF_P + sb * C::P_TILE + p_row_off;
-            float lsum = 0.f;
+            if (slow) {
+                float mx = -INFINITY;
 #pragma unroll
-            for (int q = 0; q < C::NW; ++q) {
-                if (q * 32 < p.n_mma) {
-                    uint32_t pk[16];
+                for (int q = 0; q < C::NW; ++q) {
                     if (live[q]) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float a = ex2_approx(fmaf(s[32 * q + 2 * j], kLog2e, -moff));
-                            const float bb = ex2_approx(fmaf(s[32 * q + 2 * j + 1], kLog2e, -moff));
-                            pk[j] = pack_bf16x2(a, bb);
-                            lsum += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
+                        for (int b = 0; b < 32; b += 2) {
+                            const float x0 = ((m[q] >> b) & 1u) ? s[32 * q + b] : -INFINITY;
+                            const float x1 = ((m[q] >> (b + 1)) & 1u) ? s[32 * q + b + 1] : -INFINITY;
+                            mx = max3f(mx, x0, x1);
                         }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) pk[j] = 0u;
-                    }
-#pragma unroll
-                    for (int cq = 0; cq < 4; ++cq) {
-                        const int chunk16 = q * 4 + cq;          // 8 keys = 16 bytes
-                        const uint32_t addr = prow + (chunk16 >> 3) * C::P_REG +
-                                              (((chunk16 & 7) ^ (r & 7)) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                                     "r"(pk[4 * cq]), "r"(pk[4 * cq + 1]), "r"(pk[4 * cq + 2]),
-                                     "r"(pk[4 * cq + 3])
-                                     : "memory");
                     }
                 }
+                const float mx2 = mx * kLog2e;
+                if (mx2 > m_ref + kRescaleThreshold) {
+                    if (m_ref != -INFINITY) {
+                        alpha = ex2_approx(m_ref - mx2);
+                        rescale = true;
+                    }
+                    m_ref = mx2;
+                }
+                uint32_t unused;
+                lsum = write_probabilities<C>(s, m, live, p.n_mma, m_ref == -INFINITY ? 0.f : m_ref,
+                                              t_row + C::TM_P, &unused);
             }
-            l += lsum;
-            fence_proxy_async_smem();
+            l = l * alpha + lsum;
 
             if (__any_sync(0xffffffffu, rescale)) {
-                // the previous product must have landed in O before it is scaled
-                const uint32_t gp = g - 1;
-                if (!sy.wait(sy.bar(C::B_PVDONE + (gp & 1u)), (gp >> 1) & 1u)) return;
-                tc_fence_after();
                 const float a = rescale ? alpha : 1.f;
 #pragma unroll 1
                 for (int q = 0; q < C::OPIECES; ++q) {  // HD = 16 also scales 16 unused columns
@@ -420,10 +488,10 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
                     for (int i = 0; i < 32; ++i) o[i] *= a;
                     tmem_st32(t_row + C::TM_O + q * 32, o);
                 }
-                tmem_wait_st();
             }
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(sy.bar(C::B_PFULL + sb));
+            mbar_arrive(sy.bar(C::B_PFULL));
         }
 
         // epilogue: O / l -> bf16 -> global
@@ -455,19 +523,19 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
 
 // ------------------------------------------------------------------ kernel
 
-template <int HD, int NCAP, int NS, int NQ>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int HD, int NCAP, int NS, int NQ, int CPS>
+__global__ void __launch_bounds__(kThreads, CPS)
 na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
-    using C = Cfg<HD, NCAP, NS, NQ>;
+    using C = Cfg<HD, NCAP, NS, NQ, CPS>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // Zero all tiles once: pad rows of Q and K/V tiles are never written by
-    // TMA and must hold finite values (a zero probability times NaN is NaN).
+    // Zero the Q and K/V tiles once: pad rows are never written by TMA and
+    // must hold finite values (a zero probability times NaN is NaN).
     {
         uint4* z = reinterpret_cast<uint4*>(base_ptr);
         for (int i = threadIdx.x; i < C::OFF_BAR / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
@@ -478,19 +546,19 @@ na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     Sync sy{base + C::OFF_BAR, misc + 1};
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NBAR; ++i) {
-            uint32_t cnt = 1;
-            if ((i >= C::B_SEMPTY && i < C::B_SEMPTY + 2) || (i >= C::B_PFULL && i < C::B_PFULL + 2) ||
-                i == C::B_OEMPTY)
-                cnt = 128;
+            const uint32_t cnt =
+                (i == C::B_SEMPTY || i == C::B_PFULL || i == C::B_OEMPTY) ? 128u : 1u;
             mbar_init(sy.bar(i), cnt);
         }
         misc[1] = 0u;
         fence_mbar_init();
+    }
+    if (warp == 4 && lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
     }
-    if (warp == 1) {
+    if (warp == 5) {
         tmem_alloc(base + C::OFF_MISC, C::TM_COLS);
         tmem_relinquish();
     }
@@ -499,17 +567,18 @@ na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = misc[0];
 
-    if (warp == 0) {
-        if (lane == 0) producer_role<C>(p, &tm_q, &tm_k, &tm_v, sy, base);
-    } else if (warp == 1) {
-        if (lane == 0) mma_role<C>(p, sy, base, tmem);
+    if (warp < 4) {
+        if (C::CPS == 2) regs_increase<C::REGS_HIGH>();
+        softmax_role<C>(p, sy, tmem, warp, lane);
     } else {
-        softmax_role<C>(p, sy, base, tmem, warp, lane);
+        if (C::CPS == 2) regs_decrease<C::REGS_LOW>();
+        if (warp == 4 && lane == 0) producer_role<C>(p, &tm_q, &tm_k, &tm_v, sy, base);
+        if (warp == 5 && lane == 0) mma_role<C>(p, sy, base, tmem);
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TM_COLS);
     }
@@ -517,11 +586,11 @@ na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
 // ------------------------------------------------------------------ host side
 
-template <int HD, int NCAP, int NS, int NQ>
+template <int HD, int NCAP, int NS, int NQ, int CPS>
 static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const KernelParams& kp, int grid, cudaStream_t stream) {
-    using C = Cfg<HD, NCAP, NS, NQ>;
-    auto kern = na3d_fwd_sm103<HD, NCAP, NS, NQ>;
+    using C = Cfg<HD, NCAP, NS, NQ, CPS>;
+    auto kern = na3d_fwd_sm103<HD, NCAP, NS, NQ, CPS>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
@@ -529,28 +598,29 @@ static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const 
     return cudaGetLastError();
 }
 
-template <int HD, int NCAP, int NS, int NQ>
+template <int HD, int NCAP, int NS, int NQ, int CPS>
 static void info_t(VariantInfo* v) {
-    using C = Cfg<HD, NCAP, NS, NQ>;
+    using C = Cfg<HD, NCAP, NS, NQ, CPS>;
     v->ncap = NCAP;
     v->stages = NS;
     v->hd_box = C::HDB;
     v->smem = C::SMEM_ALLOC;
+    v->ctas_per_sm = CPS;
 }
 
-// The instance table: (HD, score-tile cap, K/V stages, Q buffers).
-#define NA3D_VARIANTS(X) \
-    X(16, 128, 4, 2)     \
-    X(32, 128, 4, 2)     \
-    X(64, 128, 3, 2)     \
-    X(128, 128, 2, 1)    \
-    X(256, 64, 2, 1)
+// The instance table: (HD, score-tile cap, K/V stages, Q buffers, CTAs per SM).
+#define NA3D_VARIANTS(X)   \
+    X(16, 128, 4, 2, 2)    \
+    X(32, 128, 3, 2, 2)    \
+    X(64, 128, 2, 2, 2)    \
+    X(128, 64, 2, 1, 2)    \
+    X(256, 64, 2, 1, 1)
 
 bool variant_info(int hd, VariantInfo* info) {
     switch (hd) {
-#define X(hd_, n_, s_, q_) \
-    case hd_:              \
-        info_t<hd_, n_, s_, q_>(info); \
+#define X(hd_, n_, s_, q_, c_) \
+    case hd_:                  \
+        info_t<hd_, n_, s_, q_, c_>(info); \
         return true;
         NA3D_VARIANTS(X)
 #undef X
@@ -562,9 +632,9 @@ bool variant_info(int hd, VariantInfo* info) {
 cudaError_t launch_fwd(int hd, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const KernelParams& kp, int grid, cudaStream_t stream) {
     switch (hd) {
-#define X(hd_, n_, s_, q_) \
-    case hd_:              \
-        return launch_t<hd_, n_, s_, q_>(tq, tk, tv, kp, grid, stream);
+#define X(hd_, n_, s_, q_, c_) \
+    case hd_:                  \
+        return launch_t<hd_, n_, s_, q_, c_>(tq, tk, tv, kp, grid, stream);
         NA3D_VARIANTS(X)
 #undef X
         default:

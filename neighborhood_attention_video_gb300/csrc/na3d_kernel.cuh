@@ -24,6 +24,7 @@ struct VariantInfo {
     int stages;    // K/V pipeline depth
     int hd_box;    // head-dim columns per TMA box
     int smem;      // dynamic shared memory bytes
+    int ctas_per_sm;  // resident CTAs per SM the instance is sized for
 };
 
 bool variant_info(int hd, VariantInfo* info);
