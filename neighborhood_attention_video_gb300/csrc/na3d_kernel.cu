@@ -47,11 +47,11 @@ __device__ unsigned int g_na3d_timeout_flag = 0;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 500000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
-// The reference maximum (log2 units) is raised only when a chunk's maximum
-// exceeds it by more than this, so probabilities stay <= 2^8 and the O
-// rescale (a TMEM round trip) is rare.
+// When the maximum is recomputed, the reference maximum (log2 units) is raised
+// only if the chunk's maximum exceeds it by more than this, so the O rescale
+// (a TMEM round trip) stays rare.
 constexpr float kRescaleThreshold = 8.0f;
-constexpr uint32_t kBf16Limit = 0x4380u;   // bf16 bit pattern of 2^8
+constexpr float kSumLimit = 4294967296.0f;  // 2^32: bound on one chunk's probability sum
 constexpr int kThreads = 256;
 
 template <int HD_, int NCAP_, int NS_, int NQ_, int CPS_>
@@ -324,16 +324,14 @@ __device__ void mma_role(const KernelParams& p, const Sync& sy, uint32_t base, u
 // ------------------------------------------------------------------ softmax
 
 // P = 2^(s log2e - moff) for the masked score row (masked keys give 0), as
-// bf16 pairs into tensor memory; returns the fp32 sum of the probabilities and
-// folds the bf16 maximum into *pmax.
+// bf16 pairs into tensor memory; returns the fp32 sum of the probabilities.
 template <class C>
 __device__ __forceinline__ float write_probabilities(const float* s, const uint32_t* m,
                                                      const bool* live, int n_mma, float moff,
-                                                     uint32_t p_addr, uint32_t* pmax) {
+                                                     uint32_t p_addr) {
     const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
     const uint64_t neg2 = f2_pack(-moff, -moff);
     uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-    uint32_t mx = 0u;
 #pragma unroll
     for (int q = 0; q < C::NW; ++q) {
         if (q * 32 < n_mma) {
@@ -348,7 +346,6 @@ __device__ __forceinline__ float write_probabilities(const float* s, const uint3
                     e0 = ex2_approx(e0);
                     e1 = ex2_approx(e1);
                     pk[j] = pack_bf16x2(e0, e1);
-                    mx = bf16x2_max(mx, pk[j]);
                     if (j & 1) acc1 = f2_add(acc1, f2_pack(e0, e1));
                     else acc0 = f2_add(acc0, f2_pack(e0, e1));
                 }
@@ -359,11 +356,28 @@ __device__ __forceinline__ float write_probabilities(const float* s, const uint3
             tmem_st16(p_addr + q * 16, pk);
         }
     }
-    *pmax = mx;
     float a0, a1, b0, b1;
     f2_unpack(acc0, a0, a1);
     f2_unpack(acc1, b0, b1);
     return (a0 + a1) + (b0 + b1);
+}
+
+// Maximum of the masked score row (-inf when the row has no key here).
+template <class C>
+__device__ __forceinline__ float masked_row_max(const float* s, const uint32_t* m, const bool* live) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < C::NW; ++q) {
+        if (live[q]) {
+#pragma unroll
+            for (int b = 0; b < 32; b += 2) {
+                const float x0 = ((m[q] >> b) & 1u) ? s[32 * q + b] : -INFINITY;
+                const float x1 = ((m[q] >> (b + 1)) & 1u) ? s[32 * q + b + 1] : -INFINITY;
+                mx = max3f(mx, x0, x1);
+            }
+        }
+    }
+    return mx;
 }
 
 template <class C>
@@ -435,35 +449,24 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t tme
             if (!sy.wait(sy.bar(C::B_PVDONE), (g & 1u) ^ 1u)) return;
             tc_fence_after();
 
-            // Fast path: keep the reference maximum and check afterwards that
-            // no probability exceeded 2^8. Rows meeting their first keys, or a
-            // maximum that grew by more than 2^8, take the exact path.
+            // Fast path: probabilities against the kept reference maximum,
+            // with no max pass. A row meeting its first keys, or a chunk whose
+            // probabilities sum past 2^32 (its maximum grew by ~32 in log2
+            // units), takes the exact path: masked maximum, rescale, redo.
+            // Probabilities keep their relative precision at any scale, so
+            // both paths give the same result.
             bool slow = __any_sync(0xffffffffu, has_keys && m_ref == -INFINITY);
             float lsum = 0.f;
             if (!slow) {
-                uint32_t pmax;
                 lsum = write_probabilities<C>(s, m, live, p.n_mma, m_ref == -INFINITY ? 0.f : m_ref,
-                                              t_row + C::TM_P, &pmax);
-                const uint32_t top = max(pmax >> 16, pmax & 0xffffu);
-                slow = __any_sync(0xffffffffu, top > kBf16Limit);
-                if (slow) tmem_wait_st();
+                                              t_row + C::TM_P);
+                slow = __any_sync(0xffffffffu, !(lsum <= kSumLimit));
+                if (slow) tmem_wait_st();   // the exact path overwrites this P
             }
             float alpha = 1.f;
             bool rescale = false;
             if (slow) {
-                float mx = -INFINITY;
-#pragma unroll
-                for (int q = 0; q < C::NW; ++q) {
-                    if (live[q]) {
-#pragma unroll
-                        for (int b = 0; b < 32; b += 2) {
-                            const float x0 = ((m[q] >> b) & 1u) ? s[32 * q + b] : -INFINITY;
-                            const float x1 = ((m[q] >> (b + 1)) & 1u) ? s[32 * q + b + 1] : -INFINITY;
-                            mx = max3f(mx, x0, x1);
-                        }
-                    }
-                }
-                const float mx2 = mx * kLog2e;
+                const float mx2 = masked_row_max<C>(s, m, live) * kLog2e;
                 if (mx2 > m_ref + kRescaleThreshold) {
                     if (m_ref != -INFINITY) {
                         alpha = ex2_approx(m_ref - mx2);
@@ -471,9 +474,8 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t tme
                     }
                     m_ref = mx2;
                 }
-                uint32_t unused;
                 lsum = write_probabilities<C>(s, m, live, p.n_mma, m_ref == -INFINITY ? 0.f : m_ref,
-                                              t_row + C::TM_P, &unused);
+                                              t_row + C::TM_P);
             }
             l = l * alpha + lsum;
 
