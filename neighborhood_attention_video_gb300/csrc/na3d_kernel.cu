@@ -325,10 +325,16 @@ __device__ void mma_role(const KernelParams& p, const Sync& sy, uint32_t base, u
 
 // P = 2^(s log2e - moff) for the masked score row (masked keys give 0), as
 // bf16 pairs into tensor memory; returns the fp32 sum of the probabilities.
+//
+// P in tensor memory is still read by the previous product: the first word is
+// computed before waiting for that product (`pv_bar`, `pv_parity`), the stores
+// come after. Returns false if the wait gave up.
 template <class C>
-__device__ __forceinline__ float write_probabilities(const float* s, const uint32_t* m,
-                                                     const bool* live, int n_mma, float moff,
-                                                     uint32_t p_addr) {
+__device__ __forceinline__ bool write_probabilities(const float* s, const uint32_t* m,
+                                                    const bool* live, int n_mma, float moff,
+                                                    uint32_t p_addr, const Sync& sy,
+                                                    uint32_t pv_bar, uint32_t pv_parity,
+                                                    float* sum) {
     const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
     const uint64_t neg2 = f2_pack(-moff, -moff);
     uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
@@ -353,13 +359,18 @@ __device__ __forceinline__ float write_probabilities(const float* s, const uint3
 #pragma unroll
                 for (int j = 0; j < 16; ++j) pk[j] = 0u;
             }
+            if (q == 0) {
+                if (!sy.wait(pv_bar, pv_parity)) return false;
+                tc_fence_after();
+            }
             tmem_st16(p_addr + q * 16, pk);
         }
     }
     float a0, a1, b0, b1;
     f2_unpack(acc0, a0, a1);
     f2_unpack(acc1, b0, b1);
-    return (a0 + a1) + (b0 + b1);
+    *sum = (a0 + a1) + (b0 + b1);
+    return true;
 }
 
 // Maximum of the masked score row (-inf when the row has no key here).
@@ -445,9 +456,9 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t tme
                 live[q] = (q * 32 < p.n_mma) && __any_sync(0xffffffffu, m[q] != 0u);
             const bool has_keys = (m[0] | m[1] | m[2] | m[3]) != 0u;
 
-            // P and O are free once the previous product has completed.
-            if (!sy.wait(sy.bar(C::B_PVDONE), (g & 1u) ^ 1u)) return;
-            tc_fence_after();
+            // P and O are free once the previous product has completed
+            // (waited for inside write_probabilities, after its first word).
+            const uint32_t pv_bar = sy.bar(C::B_PVDONE), pv_parity = (g & 1u) ^ 1u;
 
             // Fast path: probabilities against the kept reference maximum,
             // with no max pass. A row meeting its first keys, or a chunk whose
@@ -458,8 +469,9 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t tme
             bool slow = __any_sync(0xffffffffu, has_keys && m_ref == -INFINITY);
             float lsum = 0.f;
             if (!slow) {
-                lsum = write_probabilities<C>(s, m, live, p.n_mma, m_ref == -INFINITY ? 0.f : m_ref,
-                                              t_row + C::TM_P);
+                if (!write_probabilities<C>(s, m, live, p.n_mma, m_ref == -INFINITY ? 0.f : m_ref,
+                                            t_row + C::TM_P, sy, pv_bar, pv_parity, &lsum))
+                    return;
                 slow = __any_sync(0xffffffffu, !(lsum <= kSumLimit));
                 if (slow) tmem_wait_st();   // the exact path overwrites this P
             }
@@ -474,8 +486,9 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t tme
                     }
                     m_ref = mx2;
                 }
-                lsum = write_probabilities<C>(s, m, live, p.n_mma, m_ref == -INFINITY ? 0.f : m_ref,
-                                              t_row + C::TM_P);
+                if (!write_probabilities<C>(s, m, live, p.n_mma, m_ref == -INFINITY ? 0.f : m_ref,
+                                            t_row + C::TM_P, sy, pv_bar, pv_parity, &lsum))
+                    return;
             }
             l = l * alpha + lsum;
 
