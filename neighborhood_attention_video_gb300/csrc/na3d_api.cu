@@ -256,6 +256,10 @@ int na3d_fwd(const void* q, const void* k, const void* v, void* out, int64_t B, 
     if (units >= (int64_t(1) << 31)) return NA3D_ERR_OVERFLOW;
     kp.n_units = int32_t(units);
     kp.out = static_cast<uint16_t*>(out);
+    kp.div_nh = na3d::make_fastdiv(kp.NH);
+    kp.div_nbw = na3d::make_fastdiv(kp.nbw);
+    kp.div_nbh = na3d::make_fastdiv(kp.nbh);
+    kp.div_nbt = na3d::make_fastdiv(kp.nbt);
 
     CUtensorMap tq, tk, tv;
     if (!encode_map(&tq, q, B, T, H, W, NH, HD, vi.hd_box, pl.bw, pl.bh, pl.bt) ||

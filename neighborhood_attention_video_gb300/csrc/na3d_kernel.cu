@@ -114,16 +114,20 @@ struct Unit {
     int n_hc, n_wc, nch;
 };
 
+// n = q * d + r for 0 <= n < 2^31 (see FastDiv).
+__device__ __forceinline__ int fast_divmod(int n, const FastDiv& f, int* r) {
+    const int q = static_cast<int>((static_cast<uint64_t>(n) * f.mul) >> f.shift);
+    *r = n - q * f.d;
+    return q;
+}
+
 __device__ __forceinline__ Unit unit_of(const KernelParams& p, int u) {
     Unit U;
-    U.n = u % p.NH;
-    u /= p.NH;
-    const int iw = u % p.nbw;
-    u /= p.nbw;
-    const int ih = u % p.nbh;
-    u /= p.nbh;
-    const int it = u % p.nbt;
-    U.b = u / p.nbt;
+    int iw, ih, it;
+    u = fast_divmod(u, p.div_nh, &U.n);
+    u = fast_divmod(u, p.div_nbw, &iw);
+    u = fast_divmod(u, p.div_nbh, &ih);
+    U.b = fast_divmod(u, p.div_nbt, &it);
     U.t0 = it * p.bt;
     U.h0 = ih * p.bh;
     U.w0 = iw * p.bw;
@@ -262,59 +266,103 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tq, cons
 
 // ------------------------------------------------------------------ tensor-core issuer
 
+// Walks the CTA's chunks in order: unit u (blockIdx.x, += gridDim.x), chunk c.
+struct ChunkWalk {
+    int u, c, nch;
+    uint32_t ul, g;   // local unit counter, global chunk counter
+    __device__ __forceinline__ void start(const KernelParams& p) {
+        u = blockIdx.x;
+        c = 0;
+        ul = 0;
+        g = 0;
+        nch = u < p.n_units ? unit_of(p, u).nch : 0;
+    }
+    __device__ __forceinline__ bool done(const KernelParams& p) const { return u >= p.n_units; }
+    __device__ __forceinline__ void next(const KernelParams& p) {
+        ++g;
+        if (++c == nch) {
+            c = 0;
+            ++ul;
+            u += gridDim.x;
+            nch = u < p.n_units ? unit_of(p, u).nch : 0;
+        }
+    }
+};
+
 template <class C>
 __device__ void mma_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem) {
     const uint32_t idesc_s = make_idesc_bf16(128, p.n_mma, 0, 0);
     const uint32_t idesc_o = make_idesc_bf16(128, C::HD, 0, 1);
-    uint32_t g = 0, ul = 0;
+    const int ksteps = p.n_mma >> 4;
 
-    // O += P_g V_g with P in tensor memory; `first` marks the unit's first
-    // product (it overwrites O).
-    auto issue_pv = [&](uint32_t gp, bool first) -> bool {
-        const uint32_t st = gp % C::NS;
-        if (first && !sy.wait(sy.bar(C::B_OEMPTY), (ul & 1u) ^ 1u)) return false;
-        if (!sy.wait(sy.bar(C::B_VFULL + st), (gp / C::NS) & 1u)) return false;
-        if (!sy.wait(sy.bar(C::B_PFULL), gp & 1u)) return false;
+    // S = Q K^T for the chunk at `w`.
+    auto issue_s = [&](const ChunkWalk& w) -> bool {
+        const uint32_t qb = w.ul % C::NQ, st = w.g % C::NS;
+        if (w.c == 0 && !sy.wait(sy.bar(C::B_QFULL + qb), (w.ul / C::NQ) & 1u)) return false;
+        if (!sy.wait(sy.bar(C::B_KFULL + st), (w.g / C::NS) & 1u)) return false;
+        if (!sy.wait(sy.bar(C::B_SEMPTY), (w.g & 1u) ^ 1u)) return false;
         tc_fence_after();
-        const uint32_t va = base + C::OFF_V + st * C::KV_TILE;
-        const int ksteps = p.n_mma >> 4;
-        for (int kk = 0; kk < ksteps; ++kk) {
-            const uint64_t bd = make_smem_desc(va + kk * 16 * C::ROWB, C::KV_REG, C::SBO, C::SWZ);
-            umma_bf16_ts(tmem + C::TM_O, tmem + C::TM_P + kk * 8, bd, idesc_o,
-                         (first && kk == 0) ? 0u : 1u);
+        const uint64_t qd = make_smem_desc(base + C::OFF_Q + qb * C::Q_TILE, 16, C::SBO, C::SWZ);
+        const uint64_t kd = make_smem_desc(base + C::OFF_K + st * C::KV_TILE, 16, C::SBO, C::SWZ);
+#pragma unroll
+        for (int kk = 0; kk < C::HD / 16; ++kk) {
+            constexpr int kPer = C::HDB / 16;   // k-steps per swizzle row
+            const uint32_t qo = ((kk / kPer) * C::Q_REG + (kk % kPer) * 32) >> 4;
+            const uint32_t ko = ((kk / kPer) * C::KV_REG + (kk % kPer) * 32) >> 4;
+            umma_bf16_ss(tmem + C::TM_S, qd + qo, kd + ko, idesc_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(sy.bar(C::B_PVDONE));
-        umma_commit(sy.bar(C::B_VEMPTY + st));
+        umma_commit(sy.bar(C::B_SFULL));
+        umma_commit(sy.bar(C::B_KEMPTY + st));
+        if (w.c == w.nch - 1) umma_commit(sy.bar(C::B_QEMPTY + qb));
         return true;
     };
 
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++ul) {
-        const Unit U = unit_of(p, u);
-        const uint32_t qb = ul % C::NQ;
-        if (!sy.wait(sy.bar(C::B_QFULL + qb), (ul / C::NQ) & 1u)) break;
-        const uint32_t qa = base + C::OFF_Q + qb * C::Q_TILE;
-        for (int c = 0; c < U.nch; ++c, ++g) {
-            const uint32_t st = g % C::NS;
-            if (!sy.wait(sy.bar(C::B_KFULL + st), (g / C::NS) & 1u)) { ok = false; break; }
-            if (!sy.wait(sy.bar(C::B_SEMPTY), (g & 1u) ^ 1u)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t ka = base + C::OFF_K + st * C::KV_TILE;
+    // O += P V for the chunk at `w`, P read from tensor memory; the unit's
+    // first product overwrites O, its last one signals the epilogue.
+    auto issue_pv = [&](const ChunkWalk& w) -> bool {
+        const uint32_t st = w.g % C::NS;
+        if (w.c == 0 && !sy.wait(sy.bar(C::B_OEMPTY), (w.ul & 1u) ^ 1u)) return false;
+        if (!sy.wait(sy.bar(C::B_VFULL + st), (w.g / C::NS) & 1u)) return false;
+        if (!sy.wait(sy.bar(C::B_PFULL), w.g & 1u)) return false;
+        tc_fence_after();
+        const uint64_t vd = make_smem_desc(base + C::OFF_V + st * C::KV_TILE, C::KV_REG, C::SBO, C::SWZ);
 #pragma unroll
-            for (int kk = 0; kk < C::HD / 16; ++kk) {
-                const int reg = kk / (C::HDB / 16), sub = kk % (C::HDB / 16);
-                const uint64_t ad = make_smem_desc(qa + reg * C::Q_REG + sub * 32, 16, C::SBO, C::SWZ);
-                const uint64_t bd = make_smem_desc(ka + reg * C::KV_REG + sub * 32, 16, C::SBO, C::SWZ);
-                umma_bf16_ss(tmem + C::TM_S, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(sy.bar(C::B_SFULL));
-            umma_commit(sy.bar(C::B_KEMPTY + st));
-            if (c == U.nch - 1) umma_commit(sy.bar(C::B_QEMPTY + qb));
-            if (c > 0 && !issue_pv(g - 1, c == 1)) { ok = false; break; }
+        for (int kk = 0; kk < C::NCAP / 16; ++kk) {
+            if (kk < ksteps)
+                umma_bf16_ts(tmem + C::TM_O, tmem + C::TM_P + kk * 8, vd + ((kk * 16 * C::ROWB) >> 4),
+                             idesc_o, (w.c == 0 && kk == 0) ? 0u : 1u);
         }
-        if (!ok) break;
-        if (!issue_pv(g - 1, U.nch == 1)) break;
-        umma_commit(sy.bar(C::B_OFULL));
+        umma_commit(sy.bar(C::B_PVDONE));
+        umma_commit(sy.bar(C::B_VEMPTY + st));
+        if (w.c == w.nch - 1) umma_commit(sy.bar(C::B_OFULL));
+        return true;
+    };
+
+    // The score tile of the next chunk is issued before the product of the
+    // current one, also across unit boundaries (the softmax then finds the
+    // next unit's first scores ready after its epilogue). With a single Q
+    // buffer the next unit's Q lands only after the current unit's last S,
+    // so there the product goes first.
+    ChunkWalk ws, wp;
+    ws.start(p);
+    wp.start(p);
+    bool ok = true;
+    if (!ws.done(p)) {
+        ok = issue_s(ws);
+        ws.next(p);
+    }
+    while (ok && !wp.done(p)) {
+        const bool s_first = !ws.done(p) && (ws.c != 0 || C::NQ > 1);
+        if (s_first) {
+            if (!issue_s(ws)) break;
+            ws.next(p);
+        }
+        if (!issue_pv(wp)) break;
+        wp.next(p);
+        if (!s_first && !ws.done(p)) {
+            if (!issue_s(ws)) break;
+            ws.next(p);
+        }
     }
     // Drain: all MMAs issued by this thread complete before TMEM is freed.
     umma_commit(sy.bar(C::B_DRAIN));

@@ -7,6 +7,25 @@
 
 namespace na3d {
 
+// Division by a runtime constant for dividends below 2^31: q = (n * mul) >> shift
+// with mul = floor(2^shift / d) + 1 and shift = 31 + ceil(log2 d), which is
+// exact for every 0 <= n < 2^31 (Granlund & Montgomery, PLDI 1994, sec. 4).
+struct FastDiv {
+    uint64_t mul;
+    uint32_t shift;
+    int32_t d;
+};
+
+inline FastDiv make_fastdiv(int32_t d) {
+    uint32_t l = 0;
+    while ((int64_t(1) << l) < d) ++l;
+    FastDiv f;
+    f.shift = 31 + l;
+    f.mul = ((uint64_t(1) << f.shift) / uint64_t(d)) + 1;
+    f.d = d;
+    return f;
+}
+
 // Everything the kernel needs besides the three TMA descriptors.
 struct KernelParams {
     int32_t B, T, H, W, NH;
@@ -16,6 +35,7 @@ struct KernelParams {
     int32_t cw, cr, n_mma;   // chunk geometry and score-tile width
     int32_t n_units;         // B * nbt * nbh * nbw * NH
     uint16_t* out;           // bf16 output, (B,T,H,W,NH,HD)
+    FastDiv div_nh, div_nbw, div_nbh, div_nbt;   // unit index decomposition
 };
 
 // Compile-time shape of one kernel instance, as the planner needs it.
