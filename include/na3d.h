@@ -95,6 +95,9 @@ typedef struct na3d_plan_info {
     int64_t bricks_per_slice;     /* bricks per (batch, head) slice */
     int64_t chunks_per_slice;     /* chunks per (batch, head) slice */
     int64_t smem_bytes;           /* dynamic shared memory per CTA */
+    int32_t w_stride;             /* 8, 16 or 32: chunk rows padded to this many keys and the
+                                     W window applied by the tensor core; 0: per-key masks */
+    int32_t reserved;
 } na3d_plan_info;
 
 /*

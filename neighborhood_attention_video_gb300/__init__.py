@@ -44,7 +44,8 @@ class PlanInfo(ctypes.Structure):
                 ("cw", ctypes.c_int32), ("cr", ctypes.c_int32), ("n_mma", ctypes.c_int32),
                 ("hd_box", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("bricks_per_slice", ctypes.c_int64), ("chunks_per_slice", ctypes.c_int64),
-                ("smem_bytes", ctypes.c_int64)]
+                ("smem_bytes", ctypes.c_int64), ("w_stride", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 def library_path() -> str:

@@ -70,26 +70,35 @@ int64_t axis_sum(int64_t N, int64_t K, int64_t b, int64_t unit, int64_t* nbricks
 
 struct Plan {
     int bt = 0, bh = 0, bw = 0, cw = 0, cr = 0, n_mma = 0;
+    int cwp = 0;   // fixed chunk stride of the tensor-core W-mask path (0: generic masks)
     int64_t bricks = 0, chunks = 0;
     double cost = 0;
 };
 
 // Costs in units of score columns of a 128-row tile: every chunk costs its
 // tile width (tensor-core and exp work) plus a fixed overhead (barriers, mask
-// set-up, MMA issue); every brick adds the epilogue and its Q load.
+// set-up, MMA issue); every brick adds the epilogue and its Q load. Columns of
+// the tensor-core W-mask path cost about half as much softmax work as columns
+// masked key by key.
 constexpr double kChunkOverhead = 24.0;
 constexpr double kBrickOverhead = 96.0;
+constexpr double kFastColumn = 0.55;
 
 Plan make_plan(int64_t T, int64_t H, int64_t W, int64_t KT, int64_t KH, int64_t KW, int ncap) {
     Plan best;
     for (int64_t bw = 1; bw <= (W < 128 ? W : 128); ++bw) {
         const int64_t ew = (bw + KW - 1 < W) ? bw + KW - 1 : W;   // widest W union
-        const int64_t cw = ew > ncap ? ncap : ew;
+        // W unions of up to 32 keys use a fixed power-of-two chunk stride and
+        // the tensor-core W mask; wider ones the generic per-key masks.
+        int64_t cwp = 0;
+        if (ew <= 32) cwp = ew <= 8 ? 8 : (ew <= 16 ? 16 : 32);
+        const int64_t cw = cwp ? cwp : (ew > ncap ? ncap : ew);
+        const double col_cost = cwp ? kFastColumn : 1.0;
         int64_t nbw;
         const int64_t sw = axis_sum(W, KW, bw, cw, &nbw);
         for (int64_t bh = 1; bh <= H && bw * bh <= 128; ++bh) {
             const int64_t eh = (bh + KH - 1 < H) ? bh + KH - 1 : H;
-            int64_t cr = ew > ncap ? 1 : ncap / cw;
+            int64_t cr = (!cwp && ew > ncap) ? 1 : ncap / cw;
             if (cr > eh) cr = eh;
             const int64_t n_mma = (cr * cw + 15) / 16 * 16;
             int64_t nbh;
@@ -99,7 +108,7 @@ Plan make_plan(int64_t T, int64_t H, int64_t W, int64_t KT, int64_t KH, int64_t 
                 const int64_t st = axis_sum(T, KT, bt, 1, &nbt);
                 const int64_t chunks = st * sh * sw;
                 const int64_t bricks = nbt * nbh * nbw;
-                const double cost = double(chunks) * (double(n_mma) + kChunkOverhead) +
+                const double cost = double(chunks) * (double(n_mma) * col_cost + kChunkOverhead) +
                                     double(bricks) * kBrickOverhead;
                 const bool better =
                     best.bt == 0 || cost < best.cost - 1e-9 ||
@@ -107,6 +116,7 @@ Plan make_plan(int64_t T, int64_t H, int64_t W, int64_t KT, int64_t KH, int64_t 
                 if (better) {
                     best.bt = int(bt); best.bh = int(bh); best.bw = int(bw);
                     best.cw = int(cw); best.cr = int(cr); best.n_mma = int(n_mma);
+                    best.cwp = int(cwp);
                     best.bricks = bricks; best.chunks = chunks; best.cost = cost;
                 }
             }
@@ -207,14 +217,16 @@ int na3d_plan(int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t K
     const int rc = validate_shape(1, T, H, W, NH, HD, KT, KH, KW);
     if (rc != NA3D_OK) return rc;
     VariantInfo vi;
-    if (!na3d::variant_info(int(HD), &vi)) return NA3D_ERR_UNSUPPORTED;
+    if (!na3d::variant_info(int(HD), 0, &vi)) return NA3D_ERR_UNSUPPORTED;
     const Plan pl = cached_plan(T, H, W, KT, KH, KW, vi.ncap);
+    if (!na3d::variant_info(int(HD), pl.cwp, &vi)) return NA3D_ERR_UNSUPPORTED;
     info->bt = pl.bt; info->bh = pl.bh; info->bw = pl.bw;
     info->cw = pl.cw; info->cr = pl.cr; info->n_mma = pl.n_mma;
     info->hd_box = vi.hd_box; info->stages = vi.stages;
     info->bricks_per_slice = pl.bricks;
     info->chunks_per_slice = pl.chunks;
     info->smem_bytes = vi.smem;
+    info->w_stride = pl.cwp;
     return NA3D_OK;
 }
 
@@ -241,8 +253,9 @@ int na3d_fwd(const void* q, const void* k, const void* v, void* out, int64_t B, 
     if (major != 10 || minor != 3) return NA3D_ERR_ARCH;
 
     VariantInfo vi;
-    if (!na3d::variant_info(int(HD), &vi)) return NA3D_ERR_UNSUPPORTED;
+    if (!na3d::variant_info(int(HD), 0, &vi)) return NA3D_ERR_UNSUPPORTED;
     const Plan pl = cached_plan(T, H, W, KT, KH, KW, vi.ncap);
+    if (!na3d::variant_info(int(HD), pl.cwp, &vi)) return NA3D_ERR_UNSUPPORTED;
 
     KernelParams kp;
     kp.B = int32_t(B); kp.T = int32_t(T); kp.H = int32_t(H); kp.W = int32_t(W); kp.NH = int32_t(NH);
@@ -269,7 +282,7 @@ int na3d_fwd(const void* q, const void* k, const void* v, void* out, int64_t B, 
 
     const int64_t slots = int64_t(sms) * vi.ctas_per_sm;   // persistent CTAs
     const int grid = int(units < slots ? units : slots);
-    if (na3d::launch_fwd(int(HD), tq, tk, tv, kp, grid, static_cast<cudaStream_t>(stream)) !=
+    if (na3d::launch_fwd(int(HD), pl.cwp, tq, tk, tv, kp, grid, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return NA3D_ERR_CUDA;
     return NA3D_OK;

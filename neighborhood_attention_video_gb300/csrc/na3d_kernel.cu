@@ -54,9 +54,24 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr float kSumLimit = 4294967296.0f;  // 2^32: bound on one chunk's probability sum
 constexpr int kThreads = 256;
 
-template <int HD_, int NCAP_, int NS_, int NQ_, int CPS_>
+// bf16 -2^40: the score offset that masks a key through the extra
+// contraction block (exact: valid keys get +0, masked ones vanish in exp2).
+constexpr uint16_t kMaskBf16 = 0xD380u;
+
+template <int HD_, int NCAP_, int NS_, int CPS_, int CWP_>
 struct Cfg {
-    static constexpr int HD = HD_, NCAP = NCAP_, NS = NS_, NQ = NQ_, CPS = CPS_;
+    static constexpr int HD = HD_, NCAP = NCAP_, NS = NS_, CPS = CPS_, CWP = CWP_;
+    // CWP > 0: chunk rows have a fixed stride of CWP keys and the W window is
+    // applied by the tensor core (extra contraction block Qx Kx^T); CWP == 0:
+    // per-element window masks in the softmax (any chunk geometry).
+    static constexpr bool FAST = CWP > 0;
+    static constexpr int KEXT = FAST ? (CWP < 16 ? 16 : CWP) : 0;   // extra contraction columns
+    static constexpr int XROWB = KEXT * 2;
+    static constexpr uint32_t XSWZ = KEXT == 32 ? kSwizzle64B : kSwizzle32B;
+    static constexpr int XSBO = 8 * XROWB;
+    static constexpr int QX_TILE = 128 * XROWB;
+    static constexpr int KX_TILE = NCAP * XROWB;
+    static constexpr int RPW = FAST ? 32 / CWP : 0;  // chunk rows per 32-column word
     static constexpr int HDB = HD < 64 ? HD : 64;   // head-dim columns per TMA box / smem row
     static constexpr int NREG = HD / HDB;           // boxes (smem regions) per tile
     static constexpr int ROWB = HDB * 2;            // bytes per smem row
@@ -68,15 +83,23 @@ struct Cfg {
     static constexpr int KV_TILE = NREG * KV_REG;
     static constexpr int NW = NCAP / 32;            // 32-column words per score row
     static constexpr int OPIECES = (HD + 31) / 32;  // 32-column TMEM loads per output row
+    // Shared memory: double-buffer Q and Qx where the per-SM share allows it.
+    static constexpr int LIMIT = (CPS == 2 ? 115712 : 232448) - 1024 - 512;
+    static constexpr int FIXED = 2 * NS * KV_TILE + (FAST ? KX_TILE : 0);
+    static constexpr int NQ = FIXED + 2 * Q_TILE + (FAST ? 2 * QX_TILE : 0) <= LIMIT ? 2 : 1;
+    static constexpr int NQX = !FAST ? 0 : (FIXED + NQ * Q_TILE + 2 * QX_TILE <= LIMIT ? 2 : 1);
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
     static constexpr int OFF_V = OFF_K + NS * KV_TILE;
-    static constexpr int OFF_BAR = OFF_V + NS * KV_TILE;
+    static constexpr int OFF_QX = OFF_V + NS * KV_TILE;
+    static constexpr int OFF_KX = OFF_QX + NQX * QX_TILE;
+    static constexpr int OFF_BAR = OFF_KX + (FAST ? KX_TILE : 0);
     // barrier indices
     static constexpr int B_QFULL = 0, B_QEMPTY = NQ;
     static constexpr int B_KFULL = 2 * NQ, B_KEMPTY = B_KFULL + NS;
     static constexpr int B_VFULL = B_KEMPTY + NS, B_VEMPTY = B_VFULL + NS;
-    static constexpr int B_SFULL = B_VEMPTY + NS, B_SEMPTY = B_SFULL + 1, B_PFULL = B_SFULL + 2,
+    static constexpr int B_XFULL = B_VEMPTY + NS, B_XEMPTY = B_XFULL + NQX;
+    static constexpr int B_SFULL = B_XEMPTY + NQX, B_SEMPTY = B_SFULL + 1, B_PFULL = B_SFULL + 2,
                          B_PVDONE = B_SFULL + 3, B_OFULL = B_SFULL + 4, B_OEMPTY = B_SFULL + 5,
                          B_DRAIN = B_SFULL + 6, NBAR = B_SFULL + 7;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -95,9 +118,10 @@ struct Cfg {
     static constexpr uint32_t REGS_HIGH = CPS == 2 ? 200 : 232;
     static_assert(CPS == 1 || (REGS_HIGH + REGS_LOW) * 128 <= REGS_LAUNCH * kThreads, "register split");
     static_assert(TM_COLS * CPS <= 512, "TMEM budget");
-    static_assert(SMEM_ALLOC * CPS <= 232448, "shared memory budget");
+    static_assert(SMEM_ALLOC * CPS <= 232448 && SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(NCAP == 64 || NCAP == 128, "score tile width");
     static_assert(NS >= 2, "K/V rings need two stages");
+    static_assert(!FAST || (CWP == 8 || CWP == 16 || CWP == 32), "fast-path chunk stride");
 };
 
 // ------------------------------------------------------------------ geometry
@@ -299,6 +323,11 @@ __device__ void mma_role(const KernelParams& p, const Sync& sy, uint32_t base, u
     auto issue_s = [&](const ChunkWalk& w) -> bool {
         const uint32_t qb = w.ul % C::NQ, st = w.g % C::NS;
         if (w.c == 0 && !sy.wait(sy.bar(C::B_QFULL + qb), (w.ul / C::NQ) & 1u)) return false;
+        uint32_t xb = 0;
+        if constexpr (C::FAST) {
+            xb = w.ul % C::NQX;
+            if (w.c == 0 && !sy.wait(sy.bar(C::B_XFULL + xb), (w.ul / C::NQX) & 1u)) return false;
+        }
         if (!sy.wait(sy.bar(C::B_KFULL + st), (w.g / C::NS) & 1u)) return false;
         if (!sy.wait(sy.bar(C::B_SEMPTY), (w.g & 1u) ^ 1u)) return false;
         tc_fence_after();
@@ -311,9 +340,19 @@ __device__ void mma_role(const KernelParams& p, const Sync& sy, uint32_t base, u
             const uint32_t ko = ((kk / kPer) * C::KV_REG + (kk % kPer) * 32) >> 4;
             umma_bf16_ss(tmem + C::TM_S, qd + qo, kd + ko, idesc_s, kk > 0 ? 1u : 0u);
         }
+        if constexpr (C::FAST) {   // S += Qx Kx^T: -2^40 on keys outside each row's W window
+            const uint64_t xd = make_smem_desc(base + C::OFF_QX + xb * C::QX_TILE, 16, C::XSBO, C::XSWZ);
+            const uint64_t yd = make_smem_desc(base + C::OFF_KX, 16, C::XSBO, C::XSWZ);
+#pragma unroll
+            for (int kk = 0; kk < C::KEXT / 16; ++kk)
+                umma_bf16_ss(tmem + C::TM_S, xd + ((kk * 32) >> 4), yd + ((kk * 32) >> 4), idesc_s, 1u);
+        }
         umma_commit(sy.bar(C::B_SFULL));
         umma_commit(sy.bar(C::B_KEMPTY + st));
-        if (w.c == w.nch - 1) umma_commit(sy.bar(C::B_QEMPTY + qb));
+        if (w.c == w.nch - 1) {
+            umma_commit(sy.bar(C::B_QEMPTY + qb));
+            if constexpr (C::FAST) umma_commit(sy.bar(C::B_XEMPTY + xb));
+        }
         return true;
     };
 
@@ -439,14 +478,130 @@ __device__ __forceinline__ float masked_row_max(const float* s, const uint32_t* 
     return mx;
 }
 
+// Byte offset of 16-byte chunk k of row `row` in a K-major operand tile with
+// rows of `rowb` bytes and the matching swizzle (the 16-byte chunk index is
+// XORed with address bits 7.. of the row start, over rowb/16 chunks).
+__device__ __forceinline__ uint32_t swizzled_chunk(int row, int k, int rowb) {
+    return static_cast<uint32_t>(row * rowb + ((k ^ (((row * rowb) >> 7) & (rowb / 16 - 1))) << 4));
+}
+
+// Probabilities for the fast path: chunk row i holds keys [i*CWP, (i+1)*CWP)
+// and is either wholly in this row's H/T window (bit i of rowbits) or not;
+// keys outside the W window already carry -2^40 from the tensor core. The
+// first word is computed before waiting for the previous product.
 template <class C>
-__device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t tmem, int warp,
-                             int lane) {
+__device__ __forceinline__ bool fast_probabilities(const float* s, uint32_t rowbits, const bool* live,
+                                                   int n_mma, float moff, uint32_t p_addr,
+                                                   const Sync& sy, uint32_t pv_bar,
+                                                   uint32_t pv_parity, float* sum) {
+    const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
+    uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+    for (int q = 0; q < C::NW; ++q) {
+        if (q * 32 < n_mma) {
+            uint32_t pk[16];
+            if (live[q]) {
+#pragma unroll
+                for (int rr = 0; rr < C::RPW; ++rr) {
+                    const int i = q * C::RPW + rr;
+                    const float nm = ((rowbits >> i) & 1u) ? -moff : -INFINITY;
+                    const uint64_t nm2 = f2_pack(nm, nm);
+#pragma unroll
+                    for (int jj = 0; jj < C::CWP / 2; ++jj) {
+                        const int j = rr * (C::CWP / 2) + jj;
+                        float e0, e1;
+                        f2_unpack(f2_fma(f2_pack(s[32 * q + 2 * j], s[32 * q + 2 * j + 1]), l2e2, nm2),
+                                  e0, e1);
+                        e0 = ex2_approx(e0);
+                        e1 = ex2_approx(e1);
+                        pk[j] = pack_bf16x2(e0, e1);
+                        if (j & 1) acc1 = f2_add(acc1, f2_pack(e0, e1));
+                        else acc0 = f2_add(acc0, f2_pack(e0, e1));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) pk[j] = 0u;
+            }
+            if (q == 0) {
+                if (!sy.wait(pv_bar, pv_parity)) return false;
+                tc_fence_after();
+            }
+            tmem_st16(p_addr + q * 16, pk);
+        }
+    }
+    float a0, a1, b0, b1;
+    f2_unpack(acc0, a0, a1);
+    f2_unpack(acc1, b0, b1);
+    *sum = (a0 + a1) + (b0 + b1);
+    return true;
+}
+
+// Maximum over the valid chunk rows (W-masked keys sit at -2^40 and never win:
+// every valid row holds the whole W window of its query).
+template <class C>
+__device__ __forceinline__ float fast_row_max(const float* s, uint32_t rowbits, const bool* live) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < C::NW; ++q) {
+        if (live[q]) {
+#pragma unroll
+            for (int rr = 0; rr < C::RPW; ++rr) {
+                const int i = q * C::RPW + rr;
+                float rm = -INFINITY;
+#pragma unroll
+                for (int jj = 0; jj < C::CWP; jj += 2) {
+                    const int b = 32 * q + rr * C::CWP + jj;
+                    rm = max3f(rm, s[b], s[b + 1]);
+                }
+                mx = ((rowbits >> i) & 1u) ? fmaxf(mx, rm) : mx;
+            }
+        }
+    }
+    return mx;
+}
+
+template <class C>
+__device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem,
+                             int warp, int lane) {
     const int r = warp * 32 + lane;             // tile row = query of the brick = TMEM lane
     const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const int M = p.bt * p.bh * p.bw;
     const int iw = r % p.bw, ih = (r / p.bw) % p.bh, it = r / (p.bw * p.bh);
     uint32_t g = 0, ul = 0;
+
+    // Qx row of unit `u` (local index `v`): -2^40 where this row's query does
+    // not see the chunk column, 0 elsewhere; published for the tensor core.
+    auto publish_qx = [&](uint32_t v, int u) -> bool {
+        if constexpr (C::FAST) {
+            const uint32_t xb = v % C::NQX;
+            if (!sy.wait(sy.bar(C::B_XEMPTY + xb), ((v / C::NQX) & 1u) ^ 1u)) return false;
+            const Unit X = unit_of(p, u);
+            const int t = X.t0 + it, h = X.h0 + ih, w = X.w0 + iw;
+            const bool ok = r < M && t < p.T && h < p.H && w < p.W;
+            const int c_lo = win_start(w, p.KW, p.W) - X.lo_w;
+            const uint32_t tile = base + C::OFF_QX + xb * C::QX_TILE;
+#pragma unroll
+            for (int k = 0; k < C::XROWB / 16; ++k) {
+                uint32_t wd[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c0 = 8 * k + 2 * e, c1 = c0 + 1;
+                    const bool m0 = ok && c0 < C::CWP && static_cast<unsigned>(c0 - c_lo) >= static_cast<unsigned>(p.KW);
+                    const bool m1 = ok && c1 < C::CWP && static_cast<unsigned>(c1 - c_lo) >= static_cast<unsigned>(p.KW);
+                    wd[e] = (m0 ? kMaskBf16 : 0u) | ((m1 ? kMaskBf16 : 0u) << 16);
+                }
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tile + swizzled_chunk(r, k, C::XROWB)),
+                             "r"(wd[0]), "r"(wd[1]), "r"(wd[2]), "r"(wd[3])
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(sy.bar(C::B_XFULL + xb));
+        }
+        return true;
+    };
+
+    if (static_cast<int>(blockIdx.x) < p.n_units && !publish_qx(0, blockIdx.x)) return;
 
     for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++ul) {
         const Unit U = unit_of(p, u);
@@ -454,16 +609,18 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t tme
         const bool valid = r < M && t < p.T && h < p.H && w < p.W;
         const int sT = win_start(t, p.KT, p.T), sH = win_start(h, p.KH, p.H),
                   sW = win_start(w, p.KW, p.W);
-        // Column pattern of this row's window inside one chunk (when a chunk
-        // holds several h-rows, the whole W extent of the halo fits in cw).
+        // Generic path: column pattern of this row's window inside one chunk
+        // (when a chunk holds several h-rows, the W extent of the halo fits in cw).
         uint32_t rowpat[4] = {0u, 0u, 0u, 0u};
-        if (p.cr > 1) {
-            const int c0 = max(sW - U.lo_w, 0), c1 = min(sW + p.KW - U.lo_w, p.cw);
-            for (int i = 0; i < p.cr; ++i) {
-                uint32_t tmp[4];
-                bit_range128(tmp, i * p.cw + c0, i * p.cw + c1);
+        if constexpr (!C::FAST) {
+            if (p.cr > 1) {
+                const int c0 = max(sW - U.lo_w, 0), c1 = min(sW + p.KW - U.lo_w, p.cw);
+                for (int i = 0; i < p.cr; ++i) {
+                    uint32_t tmp[4];
+                    bit_range128(tmp, i * p.cw + c0, i * p.cw + c1);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) rowpat[q] |= tmp[q];
+                    for (int q = 0; q < 4; ++q) rowpat[q] |= tmp[q];
+                }
             }
         }
         float m_ref = -INFINITY;   // reference maximum, log2 units
@@ -471,6 +628,41 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t tme
         ChunkCursor cur{U.lo_t, 0, 0};
 
         for (int c = 0; c < U.nch; ++c, ++g) {
+            // chunk geometry for this row (independent of the scores)
+            const int kh0 = U.lo_h + cur.hc * p.cr, kw0 = U.lo_w + cur.wc * p.cw;
+            const bool t_ok = valid && static_cast<unsigned>(cur.kt - sT) < static_cast<unsigned>(p.KT);
+            uint32_t m[4] = {0u, 0u, 0u, 0u};   // generic path: per-key mask
+            uint32_t rowbits = 0u;              // fast path: valid chunk rows
+            if (t_ok) {
+                const int i0 = max(sH - kh0, 0), i1 = min(sH + p.KH - kh0, p.cr);
+                if constexpr (C::FAST) {
+                    if (i0 < i1) rowbits = ((1u << (i1 - i0)) - 1u) << i0;
+                } else {
+                    const int c0 = max(sW - kw0, 0), c1 = min(sW + p.KW - kw0, p.cw);
+                    if (i0 < i1 && c0 < c1) {
+                        if (p.cr == 1) {
+                            bit_range128(m, c0, c1);
+                        } else {
+                            bit_range128(m, i0 * p.cw, i1 * p.cw);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) m[q] &= rowpat[q];
+                        }
+                    }
+                }
+            }
+            cur.advance(U);
+            bool live[C::NW];
+#pragma unroll
+            for (int q = 0; q < C::NW; ++q) {
+                bool mine;
+                if constexpr (C::FAST) mine = (rowbits >> (q * C::RPW)) & ((1u << C::RPW) - 1u);
+                else mine = m[q] != 0u;
+                live[q] = (q * 32 < p.n_mma) && __any_sync(0xffffffffu, mine);
+            }
+            bool has_keys;
+            if constexpr (C::FAST) has_keys = rowbits != 0u;
+            else has_keys = (m[0] | m[1] | m[2] | m[3]) != 0u;
+
             if (!sy.wait(sy.bar(C::B_SFULL), g & 1u)) return;
             tc_fence_after();
             float s[C::NCAP];
@@ -481,52 +673,38 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t tme
             tc_fence_before();
             mbar_arrive(sy.bar(C::B_SEMPTY));   // the next score tile may overwrite S now
 
-            // window mask of this row over the chunk's cr x cw keys
-            uint32_t m[4] = {0u, 0u, 0u, 0u};
-            const int kh0 = U.lo_h + cur.hc * p.cr, kw0 = U.lo_w + cur.wc * p.cw;
-            if (valid && static_cast<unsigned>(cur.kt - sT) < static_cast<unsigned>(p.KT)) {
-                const int i0 = max(sH - kh0, 0), i1 = min(sH + p.KH - kh0, p.cr);
-                const int c0 = max(sW - kw0, 0), c1 = min(sW + p.KW - kw0, p.cw);
-                if (i0 < i1 && c0 < c1) {
-                    if (p.cr == 1) {
-                        bit_range128(m, c0, c1);
-                    } else {
-                        bit_range128(m, i0 * p.cw, i1 * p.cw);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) m[q] &= rowpat[q];
-                    }
-                }
-            }
-            cur.advance(U);
-            bool live[C::NW];
-#pragma unroll
-            for (int q = 0; q < C::NW; ++q)
-                live[q] = (q * 32 < p.n_mma) && __any_sync(0xffffffffu, m[q] != 0u);
-            const bool has_keys = (m[0] | m[1] | m[2] | m[3]) != 0u;
-
             // P and O are free once the previous product has completed
-            // (waited for inside write_probabilities, after its first word).
+            // (waited for inside the probability writer, after its first word).
             const uint32_t pv_bar = sy.bar(C::B_PVDONE), pv_parity = (g & 1u) ^ 1u;
 
             // Fast path: probabilities against the kept reference maximum,
             // with no max pass. A row meeting its first keys, or a chunk whose
             // probabilities sum past 2^32 (its maximum grew by ~32 in log2
-            // units), takes the exact path: masked maximum, rescale, redo.
+            // units), takes the exact path: maximum, rescale, redo.
             // Probabilities keep their relative precision at any scale, so
             // both paths give the same result.
             bool slow = __any_sync(0xffffffffu, has_keys && m_ref == -INFINITY);
             float lsum = 0.f;
             if (!slow) {
-                if (!write_probabilities<C>(s, m, live, p.n_mma, m_ref == -INFINITY ? 0.f : m_ref,
-                                            t_row + C::TM_P, sy, pv_bar, pv_parity, &lsum))
-                    return;
+                const float moff = m_ref == -INFINITY ? 0.f : m_ref;
+                bool ok;
+                if constexpr (C::FAST)
+                    ok = fast_probabilities<C>(s, rowbits, live, p.n_mma, moff, t_row + C::TM_P, sy,
+                                               pv_bar, pv_parity, &lsum);
+                else
+                    ok = write_probabilities<C>(s, m, live, p.n_mma, moff, t_row + C::TM_P, sy,
+                                                pv_bar, pv_parity, &lsum);
+                if (!ok) return;
                 slow = __any_sync(0xffffffffu, !(lsum <= kSumLimit));
                 if (slow) tmem_wait_st();   // the exact path overwrites this P
             }
             float alpha = 1.f;
             bool rescale = false;
             if (slow) {
-                const float mx2 = masked_row_max<C>(s, m, live) * kLog2e;
+                float mx;
+                if constexpr (C::FAST) mx = fast_row_max<C>(s, rowbits, live);
+                else mx = masked_row_max<C>(s, m, live);
+                const float mx2 = mx * kLog2e;
                 if (mx2 > m_ref + kRescaleThreshold) {
                     if (m_ref != -INFINITY) {
                         alpha = ex2_approx(m_ref - mx2);
@@ -534,9 +712,15 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t tme
                     }
                     m_ref = mx2;
                 }
-                if (!write_probabilities<C>(s, m, live, p.n_mma, m_ref == -INFINITY ? 0.f : m_ref,
-                                            t_row + C::TM_P, sy, pv_bar, pv_parity, &lsum))
-                    return;
+                const float moff = m_ref == -INFINITY ? 0.f : m_ref;
+                bool ok;
+                if constexpr (C::FAST)
+                    ok = fast_probabilities<C>(s, rowbits, live, p.n_mma, moff, t_row + C::TM_P, sy,
+                                               pv_bar, pv_parity, &lsum);
+                else
+                    ok = write_probabilities<C>(s, m, live, p.n_mma, moff, t_row + C::TM_P, sy,
+                                                pv_bar, pv_parity, &lsum);
+                if (!ok) return;
             }
             l = l * alpha + lsum;
 
@@ -556,6 +740,9 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t tme
             tc_fence_before();
             mbar_arrive(sy.bar(C::B_PFULL));
         }
+
+        // the next unit's W masks go out before this unit's epilogue
+        if (u + static_cast<int>(gridDim.x) < p.n_units && !publish_qx(ul + 1, u + gridDim.x)) return;
 
         // epilogue: O / l -> bf16 -> global
         if (!sy.wait(sy.bar(C::B_OFULL), ul & 1u)) return;
@@ -586,11 +773,11 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t tme
 
 // ------------------------------------------------------------------ kernel
 
-template <int HD, int NCAP, int NS, int NQ, int CPS>
+template <int HD, int NCAP, int NS, int CPS, int CWP>
 __global__ void __launch_bounds__(kThreads, CPS)
 na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
-    using C = Cfg<HD, NCAP, NS, NQ, CPS>;
+    using C = Cfg<HD, NCAP, NS, CPS, CWP>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -601,7 +788,26 @@ na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // must hold finite values (a zero probability times NaN is NaN).
     {
         uint4* z = reinterpret_cast<uint4*>(base_ptr);
-        for (int i = threadIdx.x; i < C::OFF_BAR / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+        for (int i = threadIdx.x; i < C::OFF_KX / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    if constexpr (C::FAST) {
+        // Kx: key j of a chunk has a one in column j % CWP (its W position).
+        const int j = threadIdx.x;
+        if (j < C::NCAP) {
+#pragma unroll
+            for (int k = 0; k < C::XROWB / 16; ++k) {
+                uint32_t wd[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c0 = 8 * k + 2 * e;
+                    wd[e] = (c0 == j % CWP ? 0x3F80u : 0u) | ((c0 + 1 == j % CWP ? 0x3F80u : 0u) << 16);
+                }
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 base + C::OFF_KX + swizzled_chunk(j, k, C::XROWB)),
+                             "r"(wd[0]), "r"(wd[1]), "r"(wd[2]), "r"(wd[3])
+                             : "memory");
+            }
+        }
     }
     fence_proxy_async_smem();
 
@@ -609,9 +815,9 @@ na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     Sync sy{base + C::OFF_BAR, misc + 1};
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NBAR; ++i) {
-            const uint32_t cnt =
-                (i == C::B_SEMPTY || i == C::B_PFULL || i == C::B_OEMPTY) ? 128u : 1u;
-            mbar_init(sy.bar(i), cnt);
+            const bool softmax_arrives = i == C::B_SEMPTY || i == C::B_PFULL || i == C::B_OEMPTY ||
+                                         (i >= C::B_XFULL && i < C::B_XFULL + C::NQX);
+            mbar_init(sy.bar(i), softmax_arrives ? 128u : 1u);
         }
         misc[1] = 0u;
         fence_mbar_init();
@@ -632,7 +838,7 @@ na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     if (warp < 4) {
         if (C::CPS == 2) regs_increase<C::REGS_HIGH>();
-        softmax_role<C>(p, sy, tmem, warp, lane);
+        softmax_role<C>(p, sy, base, tmem, warp, lane);
     } else {
         if (C::CPS == 2) regs_decrease<C::REGS_LOW>();
         if (warp == 4 && lane == 0) producer_role<C>(p, &tm_q, &tm_k, &tm_v, sy, base);
@@ -649,11 +855,11 @@ na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
 // ------------------------------------------------------------------ host side
 
-template <int HD, int NCAP, int NS, int NQ, int CPS>
+template <int HD, int NCAP, int NS, int CPS, int CWP>
 static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const KernelParams& kp, int grid, cudaStream_t stream) {
-    using C = Cfg<HD, NCAP, NS, NQ, CPS>;
-    auto kern = na3d_fwd_sm103<HD, NCAP, NS, NQ, CPS>;
+    using C = Cfg<HD, NCAP, NS, CPS, CWP>;
+    auto kern = na3d_fwd_sm103<HD, NCAP, NS, CPS, CWP>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
@@ -661,9 +867,9 @@ static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const 
     return cudaGetLastError();
 }
 
-template <int HD, int NCAP, int NS, int NQ, int CPS>
+template <int HD, int NCAP, int NS, int CPS, int CWP>
 static void info_t(VariantInfo* v) {
-    using C = Cfg<HD, NCAP, NS, NQ, CPS>;
+    using C = Cfg<HD, NCAP, NS, CPS, CWP>;
     v->ncap = NCAP;
     v->stages = NS;
     v->hd_box = C::HDB;
@@ -671,38 +877,36 @@ static void info_t(VariantInfo* v) {
     v->ctas_per_sm = CPS;
 }
 
-// The instance table: (HD, score-tile cap, K/V stages, Q buffers, CTAs per SM).
-#define NA3D_VARIANTS(X)   \
-    X(16, 128, 4, 2, 2)    \
-    X(32, 128, 3, 2, 2)    \
-    X(64, 128, 2, 2, 2)    \
-    X(128, 64, 2, 1, 2)    \
-    X(256, 64, 2, 1, 1)
+// The instance table: (HD, score-tile cap, K/V stages, CTAs per SM) x chunk
+// stride CWP (0: generic masks; 8, 16, 32: W window applied by the tensor core).
+#define NA3D_HD_TABLE(X, CWP) \
+    X(16, 128, 4, 2, CWP)     \
+    X(32, 128, 3, 2, CWP)     \
+    X(64, 128, 2, 2, CWP)     \
+    X(128, 64, 2, 2, CWP)     \
+    X(256, 64, 2, 1, CWP)
+#define NA3D_VARIANTS(X) \
+    NA3D_HD_TABLE(X, 0) NA3D_HD_TABLE(X, 8) NA3D_HD_TABLE(X, 16) NA3D_HD_TABLE(X, 32)
 
-bool variant_info(int hd, VariantInfo* info) {
-    switch (hd) {
-#define X(hd_, n_, s_, q_, c_) \
-    case hd_:                  \
-        info_t<hd_, n_, s_, q_, c_>(info); \
-        return true;
-        NA3D_VARIANTS(X)
-#undef X
-        default:
-            return false;
+bool variant_info(int hd, int cwp, VariantInfo* info) {
+#define X(hd_, n_, s_, c_, w_)                   \
+    if (hd == hd_ && cwp == w_) {                \
+        info_t<hd_, n_, s_, c_, w_>(info);       \
+        return true;                             \
     }
+    NA3D_VARIANTS(X)
+#undef X
+    return false;
 }
 
-cudaError_t launch_fwd(int hd, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const KernelParams& kp, int grid, cudaStream_t stream) {
-    switch (hd) {
-#define X(hd_, n_, s_, q_, c_) \
-    case hd_:                  \
-        return launch_t<hd_, n_, s_, q_, c_>(tq, tk, tv, kp, grid, stream);
-        NA3D_VARIANTS(X)
+cudaError_t launch_fwd(int hd, int cwp, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const KernelParams& kp, int grid,
+                       cudaStream_t stream) {
+#define X(hd_, n_, s_, c_, w_) \
+    if (hd == hd_ && cwp == w_) return launch_t<hd_, n_, s_, c_, w_>(tq, tk, tv, kp, grid, stream);
+    NA3D_VARIANTS(X)
 #undef X
-        default:
-            return cudaErrorInvalidValue;
-    }
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* flag) {

@@ -47,10 +47,12 @@ struct VariantInfo {
     int ctas_per_sm;  // resident CTAs per SM the instance is sized for
 };
 
-bool variant_info(int hd, VariantInfo* info);
+// Instances exist for HD in {16, 32, 64, 128, 256} and chunk stride cwp in
+// {0 (generic per-key masks), 8, 16, 32 (W window applied by the tensor core)}.
+bool variant_info(int hd, int cwp, VariantInfo* info);
 
-// Launch the instance for `hd` on `stream` with `grid` persistent CTAs.
-cudaError_t launch_fwd(int hd, const CUtensorMap& tq, const CUtensorMap& tk,
+// Launch the instance for (hd, cwp) on `stream` with `grid` persistent CTAs.
+cudaError_t launch_fwd(int hd, int cwp, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const KernelParams& kp, int grid,
                        cudaStream_t stream);
 
