@@ -22,10 +22,10 @@
 //   warp 4      TMA producer: the Q brick once per unit; K and V of each chunk
 //               into rings of NS stages with separate barriers, K one chunk
 //               ahead of V.
-//   warp 5      tensor-core issuer: S = Q K^T (A, B in shared memory) into the
-//               TMEM score tile, then O += P V with P read from tensor memory;
-//               owns the tensor-memory allocation.
-//   warps 6, 7  idle (they complete warpgroup 1 for the register hand-over).
+//   warp 5      score issuer: S = Q K^T (+ the W-mask block) into the TMEM
+//               score tile, one chunk ahead; owns the tensor-memory allocation.
+//   warp 6      product issuer: O += P V with P read from tensor memory.
+//   warp 7      idle (it completes warpgroup 1 for the register hand-over).
 //
 // Tensor memory per CTA: S (NCAP fp32 columns), P (NCAP/2 columns of bf16
 // pairs) and O (HD columns). S is free again as soon as the softmax has read
@@ -101,7 +101,7 @@ struct Cfg {
     static constexpr int B_XFULL = B_VEMPTY + NS, B_XEMPTY = B_XFULL + NQX;
     static constexpr int B_SFULL = B_XEMPTY + NQX, B_SEMPTY = B_SFULL + 1, B_PFULL = B_SFULL + 2,
                          B_PVDONE = B_SFULL + 3, B_OFULL = B_SFULL + 4, B_OEMPTY = B_SFULL + 5,
-                         B_DRAIN = B_SFULL + 6, NBAR = B_SFULL + 7;
+                         B_DRAIN = B_SFULL + 6, B_DRAIN2 = B_SFULL + 7, NBAR = B_SFULL + 8;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
     // The floor keeps the CTA count per SM at CPS (tensor memory is sized for it).
@@ -313,39 +313,53 @@ struct ChunkWalk {
     }
 };
 
+// Score tiles: S = Q K^T (+ Qx Kx^T), one chunk after another. Issued by one
+// thread of warp 5; the products are issued by warp 6 (disjoint TMEM columns,
+// each thread commits its own MMAs), so the two streams do not wait for each
+// other's issue and sit on different SM sub-partitions.
 template <class C>
-__device__ void mma_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem) {
+__device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem) {
     const uint32_t idesc_s = make_idesc_bf16(128, p.n_mma, 0, 0);
-    const uint32_t idesc_o = make_idesc_bf16(128, C::HD, 0, 1);
-    const int ksteps = p.n_mma >> 4;
-
-    // S = Q K^T for the chunk at `w`.
-    auto issue_s = [&](const ChunkWalk& w) -> bool {
+    const uint32_t d_s = tmem + C::TM_S;
+    const uint64_t qd0 = make_smem_desc(base + C::OFF_Q, 16, C::SBO, C::SWZ);
+    const uint64_t kd0 = make_smem_desc(base + C::OFF_K, 16, C::SBO, C::SWZ);
+    const uint32_t q_hi = static_cast<uint32_t>(qd0 >> 32), k_hi = static_cast<uint32_t>(kd0 >> 32);
+    uint32_t x_hi = 0, x_lo0 = 0, y_lo = 0;
+    if constexpr (C::FAST) {
+        const uint64_t xd0 = make_smem_desc(base + C::OFF_QX, 16, C::XSBO, C::XSWZ);
+        const uint64_t yd0 = make_smem_desc(base + C::OFF_KX, 16, C::XSBO, C::XSWZ);
+        x_hi = static_cast<uint32_t>(xd0 >> 32);
+        x_lo0 = static_cast<uint32_t>(xd0);
+        y_lo = static_cast<uint32_t>(yd0);
+    }
+    ChunkWalk w;
+    w.start(p);
+    while (!w.done(p)) {
         const uint32_t qb = w.ul % C::NQ, st = w.g % C::NS;
-        if (w.c == 0 && !sy.wait(sy.bar(C::B_QFULL + qb), (w.ul / C::NQ) & 1u)) return false;
+        if (w.c == 0 && !sy.wait(sy.bar(C::B_QFULL + qb), (w.ul / C::NQ) & 1u)) break;
         uint32_t xb = 0;
         if constexpr (C::FAST) {
             xb = w.ul % C::NQX;
-            if (w.c == 0 && !sy.wait(sy.bar(C::B_XFULL + xb), (w.ul / C::NQX) & 1u)) return false;
+            if (w.c == 0 && !sy.wait(sy.bar(C::B_XFULL + xb), (w.ul / C::NQX) & 1u)) break;
         }
-        if (!sy.wait(sy.bar(C::B_KFULL + st), (w.g / C::NS) & 1u)) return false;
-        if (!sy.wait(sy.bar(C::B_SEMPTY), (w.g & 1u) ^ 1u)) return false;
+        if (!sy.wait(sy.bar(C::B_KFULL + st), (w.g / C::NS) & 1u)) break;
+        if (!sy.wait(sy.bar(C::B_SEMPTY), (w.g & 1u) ^ 1u)) break;
         tc_fence_after();
-        const uint64_t qd = make_smem_desc(base + C::OFF_Q + qb * C::Q_TILE, 16, C::SBO, C::SWZ);
-        const uint64_t kd = make_smem_desc(base + C::OFF_K + st * C::KV_TILE, 16, C::SBO, C::SWZ);
+        const uint32_t q_lo = static_cast<uint32_t>(qd0) + ((qb * C::Q_TILE) >> 4);
+        const uint32_t k_lo = static_cast<uint32_t>(kd0) + ((st * C::KV_TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::HD / 16; ++kk) {
             constexpr int kPer = C::HDB / 16;   // k-steps per swizzle row
             const uint32_t qo = ((kk / kPer) * C::Q_REG + (kk % kPer) * 32) >> 4;
             const uint32_t ko = ((kk / kPer) * C::KV_REG + (kk % kPer) * 32) >> 4;
-            umma_bf16_ss(tmem + C::TM_S, qd + qo, kd + ko, idesc_s, kk > 0 ? 1u : 0u);
+            if (kk == 0) umma_ss_halves<0>(d_s, q_lo + qo, q_hi, k_lo + ko, k_hi, idesc_s);
+            else umma_ss_halves<1>(d_s, q_lo + qo, q_hi, k_lo + ko, k_hi, idesc_s);
         }
         if constexpr (C::FAST) {   // S += Qx Kx^T: -2^40 on keys outside each row's W window
-            const uint64_t xd = make_smem_desc(base + C::OFF_QX + xb * C::QX_TILE, 16, C::XSBO, C::XSWZ);
-            const uint64_t yd = make_smem_desc(base + C::OFF_KX, 16, C::XSBO, C::XSWZ);
+            const uint32_t x_lo = x_lo0 + ((xb * C::QX_TILE) >> 4);
 #pragma unroll
             for (int kk = 0; kk < C::KEXT / 16; ++kk)
-                umma_bf16_ss(tmem + C::TM_S, xd + ((kk * 32) >> 4), yd + ((kk * 32) >> 4), idesc_s, 1u);
+                umma_ss_halves<1>(d_s, x_lo + kk * 2, x_hi, y_lo + kk * 2, x_hi, idesc_s);
         }
         umma_commit(sy.bar(C::B_SFULL));
         umma_commit(sy.bar(C::B_KEMPTY + st));
@@ -353,59 +367,44 @@ __device__ void mma_role(const KernelParams& p, const Sync& sy, uint32_t base, u
             umma_commit(sy.bar(C::B_QEMPTY + qb));
             if constexpr (C::FAST) umma_commit(sy.bar(C::B_XEMPTY + xb));
         }
-        return true;
-    };
-
-    // O += P V for the chunk at `w`, P read from tensor memory; the unit's
-    // first product overwrites O, its last one signals the epilogue.
-    auto issue_pv = [&](const ChunkWalk& w) -> bool {
-        const uint32_t st = w.g % C::NS;
-        if (w.c == 0 && !sy.wait(sy.bar(C::B_OEMPTY), (w.ul & 1u) ^ 1u)) return false;
-        if (!sy.wait(sy.bar(C::B_VFULL + st), (w.g / C::NS) & 1u)) return false;
-        if (!sy.wait(sy.bar(C::B_PFULL), w.g & 1u)) return false;
-        tc_fence_after();
-        const uint64_t vd = make_smem_desc(base + C::OFF_V + st * C::KV_TILE, C::KV_REG, C::SBO, C::SWZ);
-#pragma unroll
-        for (int kk = 0; kk < C::NCAP / 16; ++kk) {
-            if (kk < ksteps)
-                umma_bf16_ts(tmem + C::TM_O, tmem + C::TM_P + kk * 8, vd + ((kk * 16 * C::ROWB) >> 4),
-                             idesc_o, (w.c == 0 && kk == 0) ? 0u : 1u);
-        }
-        umma_commit(sy.bar(C::B_PVDONE));
-        umma_commit(sy.bar(C::B_VEMPTY + st));
-        if (w.c == w.nch - 1) umma_commit(sy.bar(C::B_OFULL));
-        return true;
-    };
-
-    // The score tile of the next chunk is issued before the product of the
-    // current one, also across unit boundaries (the softmax then finds the
-    // next unit's first scores ready after its epilogue). With a single Q
-    // buffer the next unit's Q lands only after the current unit's last S,
-    // so there the product goes first.
-    ChunkWalk ws, wp;
-    ws.start(p);
-    wp.start(p);
-    bool ok = true;
-    if (!ws.done(p)) {
-        ok = issue_s(ws);
-        ws.next(p);
-    }
-    while (ok && !wp.done(p)) {
-        const bool s_first = !ws.done(p) && (ws.c != 0 || C::NQ > 1);
-        if (s_first) {
-            if (!issue_s(ws)) break;
-            ws.next(p);
-        }
-        if (!issue_pv(wp)) break;
-        wp.next(p);
-        if (!s_first && !ws.done(p)) {
-            if (!issue_s(ws)) break;
-            ws.next(p);
-        }
+        w.next(p);
     }
     // Drain: all MMAs issued by this thread complete before TMEM is freed.
     umma_commit(sy.bar(C::B_DRAIN));
     mbar_wait_bounded(sy.bar(C::B_DRAIN), 0, kDrainLimitNs);
+}
+
+// Products: O += P V with P read from tensor memory; the unit's first
+// product overwrites O, its last one signals the epilogue.
+template <class C>
+__device__ void mma_pv_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem) {
+    const uint32_t idesc_o = make_idesc_bf16(128, C::HD, 0, 1);
+    const uint32_t d_o = tmem + C::TM_O, a_p = tmem + C::TM_P;
+    const uint64_t vd0 = make_smem_desc(base + C::OFF_V, C::KV_REG, C::SBO, C::SWZ);
+    const uint32_t v_hi = static_cast<uint32_t>(vd0 >> 32);
+    const int ksteps = p.n_mma >> 4;
+    ChunkWalk w;
+    w.start(p);
+    while (!w.done(p)) {
+        const uint32_t st = w.g % C::NS;
+        if (w.c == 0 && !sy.wait(sy.bar(C::B_OEMPTY), (w.ul & 1u) ^ 1u)) break;
+        if (!sy.wait(sy.bar(C::B_VFULL + st), (w.g / C::NS) & 1u)) break;
+        if (!sy.wait(sy.bar(C::B_PFULL), w.g & 1u)) break;
+        tc_fence_after();
+        const uint32_t v_lo = static_cast<uint32_t>(vd0) + ((st * C::KV_TILE) >> 4);
+        if (w.c == 0) umma_ts_halves<0>(d_o, a_p, v_lo, v_hi, idesc_o);
+        else umma_ts_halves<1>(d_o, a_p, v_lo, v_hi, idesc_o);
+#pragma unroll
+        for (int kk = 1; kk < C::NCAP / 16; ++kk)
+            if (kk < ksteps)
+                umma_ts_halves<1>(d_o, a_p + kk * 8, v_lo + ((kk * 16 * C::ROWB) >> 4), v_hi, idesc_o);
+        umma_commit(sy.bar(C::B_PVDONE));
+        umma_commit(sy.bar(C::B_VEMPTY + st));
+        if (w.c == w.nch - 1) umma_commit(sy.bar(C::B_OFULL));
+        w.next(p);
+    }
+    umma_commit(sy.bar(C::B_DRAIN2));
+    mbar_wait_bounded(sy.bar(C::B_DRAIN2), 0, kDrainLimitNs);
 }
 
 // ------------------------------------------------------------------ softmax
@@ -842,7 +841,8 @@ na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     } else {
         if (C::CPS == 2) regs_decrease<C::REGS_LOW>();
         if (warp == 4 && lane == 0) producer_role<C>(p, &tm_q, &tm_k, &tm_v, sy, base);
-        if (warp == 5 && lane == 0) mma_role<C>(p, sy, base, tmem);
+        if (warp == 5 && lane == 0) mma_s_role<C>(p, sy, base, tmem);
+        if (warp == 6 && lane == 0) mma_pv_role<C>(p, sy, base, tmem);
     }
 
     tc_fence_before();
