@@ -14,27 +14,23 @@
 // one frame (t), loaded with one TMA box per 64 head-dim columns. Queries are
 // the M = 128 rows of every tensor-core tile; a chunk's keys are its N columns.
 //
-// Roles (384 threads, one CTA per SM):
-//   warps 0..7  softmax (warpgroups 0 and 1): warps w and w+4 share the 32
-//               TMEM lanes (query rows) of sub-partition w, each taking half of
-//               the score columns: window mask, probabilities into tensor
-//               memory, running sums, occasional O rescale, and the epilogue
-//               O / l -> bf16 -> HBM for half of the head dimension. The two
-//               halves of a row agree through a 64-thread named barrier.
-//   warp 8      TMA producer: the Q brick once per unit; K and V of each chunk
+// Roles (256 threads; two CTAs per SM for HD <= 128, one for HD = 256):
+//   warps 0..3  softmax (warpgroup 0): one query row per thread (its TMEM
+//               lane): window mask, running max and sum in log2 space, P as
+//               bf16 into tensor memory, occasional O rescale, and the
+//               epilogue O / l -> bf16 -> HBM.
+//   warp 4      TMA producer: the Q brick once per unit; K and V of each chunk
 //               into rings of NS stages with separate barriers, K one chunk
 //               ahead of V.
-//   warp 9      score issuer: S = Q K^T (+ the W-mask block) into one of two
-//               TMEM score tiles; owns the tensor-memory allocation.
-//   warp 10     product issuer: O += P V with P read from one of two TMEM
-//               probability tiles.
-//   warp 11     idle (it completes warpgroup 2 for the register hand-over).
+//   warp 5      score issuer: S = Q K^T (+ the W-mask block) into the TMEM
+//               score tile, one chunk ahead; owns the tensor-memory allocation.
+//   warp 6      product issuer: O += P V with P read from tensor memory.
+//   warp 7      idle (it completes warpgroup 1 for the register hand-over).
 //
-// Tensor memory: S (2 x NCAP fp32 columns), P (2 x NCAP/2 columns of bf16
-// pairs), O (HD fp32 columns). With both tiles doubled, the score tile of the
-// next chunk is computed while the softmax works on the current one, and the
-// softmax writes the next probabilities while the tensor core still reads the
-// previous ones.
+// Tensor memory per CTA: S (NCAP fp32 columns), P (NCAP/2 columns of bf16
+// pairs) and O (HD columns). S is free again as soon as the softmax has read
+// it into registers, so the next score tile is computed while the softmax
+// works on the current one.
 //
 // Every pipeline wait is bounded: a wait that runs out sets a device flag, all
 // roles drop out of their loops, in-flight copies and MMAs are drained, and
@@ -56,14 +52,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 // (a TMEM round trip) stays rare.
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kSumLimit = 4294967296.0f;  // 2^32: bound on one chunk's probability sum
-constexpr int kThreads = 384;
+constexpr int kThreads = 256;
+
 // bf16 -2^40: the score offset that masks a key through the extra
 // contraction block (exact: valid keys get +0, masked ones vanish in exp2).
 constexpr uint16_t kMaskBf16 = 0xD380u;
 
-template <int HD_, int NCAP_, int CWP_>
+template <int HD_, int NCAP_, int NS_, int CPS_, int CWP_>
 struct Cfg {
-    static constexpr int HD = HD_, NCAP = NCAP_, CWP = CWP_;
+    static constexpr int HD = HD_, NCAP = NCAP_, NS = NS_, CPS = CPS_, CWP = CWP_;
     // CWP > 0: chunk rows have a fixed stride of CWP keys and the W window is
     // applied by the tensor core (extra contraction block Qx Kx^T); CWP == 0:
     // per-element window masks in the softmax (any chunk geometry).
@@ -85,52 +82,43 @@ struct Cfg {
     static constexpr int KV_REG = NCAP * ROWB;
     static constexpr int KV_TILE = NREG * KV_REG;
     static constexpr int NW = NCAP / 32;            // 32-column words per score row
-    static constexpr int NWH = NW / 2;              // words per half row
     static constexpr int OPIECES = (HD + 31) / 32;  // 32-column TMEM loads per output row
-    static constexpr int OPH = (OPIECES + 1) / 2;   // output pieces per half
-    // Shared memory: as many K/V stages and Q/Qx buffers as fit.
-    static constexpr int XCH_BYTES = 5 * 1024;      // max / flag / sum exchange between row halves
-    static constexpr int LIMIT = 232448 - 1024 - 512 - XCH_BYTES;
-    static constexpr int FX = FAST ? KX_TILE : 0, QXT = FAST ? QX_TILE : 0;
-    static constexpr int NS = (2 * 4 * KV_TILE + FX + 2 * Q_TILE + 2 * QXT <= LIMIT) ? 4
-                            : (2 * 3 * KV_TILE + FX + 2 * Q_TILE + 2 * QXT <= LIMIT) ? 3 : 2;
-    static constexpr int FIXED = 2 * NS * KV_TILE + FX;
-    static constexpr int NQ = FIXED + 2 * Q_TILE + 2 * QXT <= LIMIT ? 2 : 1;
+    // Shared memory: double-buffer Q and Qx where the per-SM share allows it.
+    static constexpr int LIMIT = (CPS == 2 ? 115712 : 232448) - 1024 - 512;
+    static constexpr int FIXED = 2 * NS * KV_TILE + (FAST ? KX_TILE : 0);
+    static constexpr int NQ = FIXED + 2 * Q_TILE + (FAST ? 2 * QX_TILE : 0) <= LIMIT ? 2 : 1;
     static constexpr int NQX = !FAST ? 0 : (FIXED + NQ * Q_TILE + 2 * QX_TILE <= LIMIT ? 2 : 1);
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
     static constexpr int OFF_V = OFF_K + NS * KV_TILE;
     static constexpr int OFF_QX = OFF_V + NS * KV_TILE;
     static constexpr int OFF_KX = OFF_QX + NQX * QX_TILE;
-    static constexpr int OFF_XCH = OFF_KX + FX;
-    static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
+    static constexpr int OFF_BAR = OFF_KX + (FAST ? KX_TILE : 0);
     // barrier indices
     static constexpr int B_QFULL = 0, B_QEMPTY = NQ;
     static constexpr int B_KFULL = 2 * NQ, B_KEMPTY = B_KFULL + NS;
     static constexpr int B_VFULL = B_KEMPTY + NS, B_VEMPTY = B_VFULL + NS;
     static constexpr int B_XFULL = B_VEMPTY + NS, B_XEMPTY = B_XFULL + NQX;
-    static constexpr int B_SFULL = B_XEMPTY + NQX;    // [2]
-    static constexpr int B_SEMPTY = B_SFULL + 2;      // [2]
-    static constexpr int B_PFULL = B_SEMPTY + 2;      // [2]
-    static constexpr int B_PVDONE = B_PFULL + 2;      // [2]
-    static constexpr int B_OFULL = B_PVDONE + 2, B_OEMPTY = B_OFULL + 1, B_DRAIN = B_OFULL + 2,
-                         B_DRAIN2 = B_OFULL + 3, B_PAIR = B_OFULL + 4, NBAR = B_PAIR + 4;
+    static constexpr int B_SFULL = B_XEMPTY + NQX, B_SEMPTY = B_SFULL + 1, B_PFULL = B_SFULL + 2,
+                         B_PVDONE = B_SFULL + 3, B_OFULL = B_SFULL + 4, B_OEMPTY = B_SFULL + 5,
+                         B_DRAIN = B_SFULL + 6, B_DRAIN2 = B_SFULL + 7, NBAR = B_SFULL + 8;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
-    static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
-    static constexpr uint32_t TM_S = 0;                    // 2 x NCAP fp32 score columns
-    static constexpr uint32_t TM_P = 2 * NCAP;             // 2 x NCAP / 2 columns of bf16 pairs
-    static constexpr uint32_t TM_O = 3 * NCAP;             // HD fp32 output columns
+    // The floor keeps the CTA count per SM at CPS (tensor memory is sized for it).
+    static constexpr int MIN_SMEM = CPS == 2 ? 80 * 1024 : 120 * 1024;
+    static constexpr int SMEM_ALLOC = (SMEM_USED + 1024) > MIN_SMEM ? (SMEM_USED + 1024) : MIN_SMEM;
+    static constexpr uint32_t TM_S = 0;                    // NCAP fp32 score columns
+    static constexpr uint32_t TM_P = NCAP;                 // NCAP / 2 columns of bf16 pairs
+    static constexpr uint32_t TM_O = NCAP + NCAP / 2;      // HD fp32 output columns
     static constexpr uint32_t TM_NEED = TM_O + OPIECES * 32;
     static constexpr uint32_t TM_COLS = TM_NEED <= 256 ? 256 : 512;
-    // registers: warpgroup 2 (producer, issuers) gives its share to the two
-    // softmax warpgroups
-    static constexpr uint32_t REGS_LAUNCH = 168;
-    static constexpr uint32_t REGS_LOW = 88;
-    static constexpr uint32_t REGS_HIGH = 208;
-    static_assert((2 * REGS_HIGH + REGS_LOW) * 128 <= REGS_LAUNCH * kThreads, "register split");
-    static_assert(TM_NEED <= 512, "TMEM budget");
-    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    // registers: warpgroup 1 gives its share to the softmax warpgroup
+    static constexpr uint32_t REGS_LAUNCH = 65536 / (kThreads * CPS) >= 256 ? 255 : 65536 / (kThreads * CPS);
+    static constexpr uint32_t REGS_LOW = 56;
+    static constexpr uint32_t REGS_HIGH = CPS == 2 ? 200 : 232;
+    static_assert(CPS == 1 || (REGS_HIGH + REGS_LOW) * 128 <= REGS_LAUNCH * kThreads, "register split");
+    static_assert(TM_COLS * CPS <= 512, "TMEM budget");
+    static_assert(SMEM_ALLOC * CPS <= 232448 && SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(NCAP == 64 || NCAP == 128, "score tile width");
     static_assert(NS >= 2, "K/V rings need two stages");
     static_assert(!FAST || (CWP == 8 || CWP == 16 || CWP == 32), "fast-path chunk stride");
@@ -300,7 +288,7 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tq, cons
     }
 }
 
-// ------------------------------------------------------------------ tensor-core issuers
+// ------------------------------------------------------------------ tensor-core issuer
 
 // Walks the CTA's chunks in order: unit u (blockIdx.x, += gridDim.x), chunk c.
 struct ChunkWalk {
@@ -325,13 +313,14 @@ struct ChunkWalk {
     }
 };
 
-// Score tiles: S = Q K^T (+ Qx Kx^T) into alternating TMEM tiles, one chunk
-// after another. Issued by one thread of warp 9; the products are issued by
-// warp 10 (disjoint TMEM columns, each thread commits its own MMAs), so the
-// two streams do not wait for each other's issue.
+// Score tiles: S = Q K^T (+ Qx Kx^T), one chunk after another. Issued by one
+// thread of warp 5; the products are issued by warp 6 (disjoint TMEM columns,
+// each thread commits its own MMAs), so the two streams do not wait for each
+// other's issue and sit on different SM sub-partitions.
 template <class C>
 __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem) {
     const uint32_t idesc_s = make_idesc_bf16(128, p.n_mma, 0, 0);
+    const uint32_t d_s = tmem + C::TM_S;
     const uint64_t qd0 = make_smem_desc(base + C::OFF_Q, 16, C::SBO, C::SWZ);
     const uint64_t kd0 = make_smem_desc(base + C::OFF_K, 16, C::SBO, C::SWZ);
     const uint32_t q_hi = static_cast<uint32_t>(qd0 >> 32), k_hi = static_cast<uint32_t>(kd0 >> 32);
@@ -346,7 +335,7 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
     ChunkWalk w;
     w.start(p);
     while (!w.done(p)) {
-        const uint32_t qb = w.ul % C::NQ, st = w.g % C::NS, sb = w.g & 1u;
+        const uint32_t qb = w.ul % C::NQ, st = w.g % C::NS;
         if (w.c == 0 && !sy.wait(sy.bar(C::B_QFULL + qb), (w.ul / C::NQ) & 1u)) break;
         uint32_t xb = 0;
         if constexpr (C::FAST) {
@@ -354,9 +343,8 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
             if (w.c == 0 && !sy.wait(sy.bar(C::B_XFULL + xb), (w.ul / C::NQX) & 1u)) break;
         }
         if (!sy.wait(sy.bar(C::B_KFULL + st), (w.g / C::NS) & 1u)) break;
-        if (!sy.wait(sy.bar(C::B_SEMPTY + sb), ((w.g >> 1) & 1u) ^ 1u)) break;
+        if (!sy.wait(sy.bar(C::B_SEMPTY), (w.g & 1u) ^ 1u)) break;
         tc_fence_after();
-        const uint32_t d_s = tmem + C::TM_S + sb * C::NCAP;
         const uint32_t q_lo = static_cast<uint32_t>(qd0) + ((qb * C::Q_TILE) >> 4);
         const uint32_t k_lo = static_cast<uint32_t>(kd0) + ((st * C::KV_TILE) >> 4);
 #pragma unroll
@@ -373,7 +361,7 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
             for (int kk = 0; kk < C::KEXT / 16; ++kk)
                 umma_ss_halves<1>(d_s, x_lo + kk * 2, x_hi, y_lo + kk * 2, x_hi, idesc_s);
         }
-        umma_commit(sy.bar(C::B_SFULL + sb));
+        umma_commit(sy.bar(C::B_SFULL));
         umma_commit(sy.bar(C::B_KEMPTY + st));
         if (w.c == w.nch - 1) {
             umma_commit(sy.bar(C::B_QEMPTY + qb));
@@ -386,24 +374,23 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
     mbar_wait_bounded(sy.bar(C::B_DRAIN), 0, kDrainLimitNs);
 }
 
-// Products: O += P V with P read from one of the two TMEM probability tiles;
-// the unit's first product overwrites O, its last one signals the epilogue.
+// Products: O += P V with P read from tensor memory; the unit's first
+// product overwrites O, its last one signals the epilogue.
 template <class C>
 __device__ void mma_pv_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem) {
     const uint32_t idesc_o = make_idesc_bf16(128, C::HD, 0, 1);
-    const uint32_t d_o = tmem + C::TM_O;
+    const uint32_t d_o = tmem + C::TM_O, a_p = tmem + C::TM_P;
     const uint64_t vd0 = make_smem_desc(base + C::OFF_V, C::KV_REG, C::SBO, C::SWZ);
     const uint32_t v_hi = static_cast<uint32_t>(vd0 >> 32);
     const int ksteps = p.n_mma >> 4;
     ChunkWalk w;
     w.start(p);
     while (!w.done(p)) {
-        const uint32_t st = w.g % C::NS, pb = w.g & 1u;
+        const uint32_t st = w.g % C::NS;
         if (w.c == 0 && !sy.wait(sy.bar(C::B_OEMPTY), (w.ul & 1u) ^ 1u)) break;
         if (!sy.wait(sy.bar(C::B_VFULL + st), (w.g / C::NS) & 1u)) break;
-        if (!sy.wait(sy.bar(C::B_PFULL + pb), (w.g >> 1) & 1u)) break;
+        if (!sy.wait(sy.bar(C::B_PFULL), w.g & 1u)) break;
         tc_fence_after();
-        const uint32_t a_p = tmem + C::TM_P + pb * (C::NCAP / 2);
         const uint32_t v_lo = static_cast<uint32_t>(vd0) + ((st * C::KV_TILE) >> 4);
         if (w.c == 0) umma_ts_halves<0>(d_o, a_p, v_lo, v_hi, idesc_o);
         else umma_ts_halves<1>(d_o, a_p, v_lo, v_hi, idesc_o);
@@ -411,7 +398,7 @@ __device__ void mma_pv_role(const KernelParams& p, const Sync& sy, uint32_t base
         for (int kk = 1; kk < C::NCAP / 16; ++kk)
             if (kk < ksteps)
                 umma_ts_halves<1>(d_o, a_p + kk * 8, v_lo + ((kk * 16 * C::ROWB) >> 4), v_hi, idesc_o);
-        umma_commit(sy.bar(C::B_PVDONE + pb));
+        umma_commit(sy.bar(C::B_PVDONE));
         umma_commit(sy.bar(C::B_VEMPTY + st));
         if (w.c == w.nch - 1) umma_commit(sy.bar(C::B_OFULL));
         w.next(p);
@@ -422,118 +409,30 @@ __device__ void mma_pv_role(const KernelParams& p, const Sync& sy, uint32_t base
 
 // ------------------------------------------------------------------ softmax
 
-// Byte offset of 16-byte chunk k of row `row` in a K-major operand tile with
-// rows of `rowb` bytes and the matching swizzle (the 16-byte chunk index is
-// XORed with address bits 7.. of the row start, over rowb/16 chunks).
-__device__ __forceinline__ uint32_t swizzled_chunk(int row, int k, int rowb) {
-    return static_cast<uint32_t>(row * rowb + ((k ^ (((row * rowb) >> 7) & (rowb / 16 - 1))) << 4));
-}
-
-// Everything one softmax thread needs to turn its half of a score row into
-// probabilities. Word index q is global (0..NW-1); this thread owns words
-// [q0, q0 + NWH) and holds their scores in s[0 .. 32*NWH).
-struct RowHalf {
-    int q0;
-    int n_mma;
-    uint32_t p_addr;       // TMEM address of this lane's probability tile (column 0)
-    uint32_t pv_bar, pv_parity;
-};
-
-// Probabilities of the fast path: chunk row i holds keys [i*CWP, (i+1)*CWP)
-// and is either wholly in this row's H/T window (bit i of rowbits) or not;
-// keys outside the W window already carry -2^40 from the tensor core. The
-// first word is computed before waiting for the tile to be free.
+// P = 2^(s log2e - moff) for the masked score row (masked keys give 0), as
+// bf16 pairs into tensor memory; returns the fp32 sum of the probabilities.
+//
+// P in tensor memory is still read by the previous product: the first word is
+// computed before waiting for that product (`pv_bar`, `pv_parity`), the stores
+// come after. Returns false if the wait gave up.
 template <class C>
-__device__ __forceinline__ bool fast_probabilities(const float* s, uint32_t rowbits, const bool* live,
-                                                   float moff, const RowHalf& rh, const Sync& sy,
-                                                   float* sum) {
-    const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
-    uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-#pragma unroll
-    for (int ql = 0; ql < C::NWH; ++ql) {
-        const int q = rh.q0 + ql;
-        if (q * 32 < rh.n_mma) {
-            uint32_t pk[16];
-            if (live[ql]) {
-#pragma unroll
-                for (int rr = 0; rr < C::RPW; ++rr) {
-                    const int i = q * C::RPW + rr;
-                    const float nm = ((rowbits >> i) & 1u) ? -moff : -INFINITY;
-                    const uint64_t nm2 = f2_pack(nm, nm);
-#pragma unroll
-                    for (int jj = 0; jj < C::CWP / 2; ++jj) {
-                        const int j = rr * (C::CWP / 2) + jj;
-                        float e0, e1;
-                        f2_unpack(f2_fma(f2_pack(s[32 * ql + 2 * j], s[32 * ql + 2 * j + 1]), l2e2, nm2),
-                                  e0, e1);
-                        e0 = ex2_approx(e0);
-                        e1 = ex2_approx(e1);
-                        pk[j] = pack_bf16x2(e0, e1);
-                        if (j & 1) acc1 = f2_add(acc1, f2_pack(e0, e1));
-                        else acc0 = f2_add(acc0, f2_pack(e0, e1));
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) pk[j] = 0u;
-            }
-            if (ql == 0) {
-                if (!sy.wait(rh.pv_bar, rh.pv_parity)) return false;
-                tc_fence_after();
-            }
-            tmem_st16(rh.p_addr + q * 16, pk);
-        }
-    }
-    float a0, a1, b0, b1;
-    f2_unpack(acc0, a0, a1);
-    f2_unpack(acc1, b0, b1);
-    *sum = (a0 + a1) + (b0 + b1);
-    return true;
-}
-
-// Maximum of this half over the valid chunk rows (W-masked keys sit at -2^40
-// and never win: every valid row holds the whole W window of its query).
-template <class C>
-__device__ __forceinline__ float fast_half_max(const float* s, uint32_t rowbits, const bool* live, int q0) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int ql = 0; ql < C::NWH; ++ql) {
-        if (live[ql]) {
-#pragma unroll
-            for (int rr = 0; rr < C::RPW; ++rr) {
-                const int i = (q0 + ql) * C::RPW + rr;
-                float rm = -INFINITY;
-#pragma unroll
-                for (int jj = 0; jj < C::CWP; jj += 2) {
-                    const int b = 32 * ql + rr * C::CWP + jj;
-                    rm = max3f(rm, s[b], s[b + 1]);
-                }
-                mx = ((rowbits >> i) & 1u) ? fmaxf(mx, rm) : mx;
-            }
-        }
-    }
-    return mx;
-}
-
-// Probabilities of the generic path: per-key masks m[ql] (one bit per score
-// column of word q0 + ql).
-template <class C>
-__device__ __forceinline__ bool masked_probabilities(const float* s, const uint32_t* m, const bool* live,
-                                                     float moff, const RowHalf& rh, const Sync& sy,
-                                                     float* sum) {
+__device__ __forceinline__ bool write_probabilities(const float* s, const uint32_t* m,
+                                                    const bool* live, int n_mma, float moff,
+                                                    uint32_t p_addr, const Sync& sy,
+                                                    uint32_t pv_bar, uint32_t pv_parity,
+                                                    float* sum) {
     const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
     const uint64_t neg2 = f2_pack(-moff, -moff);
     uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-    for (int ql = 0; ql < C::NWH; ++ql) {
-        const int q = rh.q0 + ql;
-        if (q * 32 < rh.n_mma) {
+    for (int q = 0; q < C::NW; ++q) {
+        if (q * 32 < n_mma) {
             uint32_t pk[16];
-            if (live[ql]) {
+            if (live[q]) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float x0 = ((m[ql] >> (2 * j)) & 1u) ? s[32 * ql + 2 * j] : -INFINITY;
-                    const float x1 = ((m[ql] >> (2 * j + 1)) & 1u) ? s[32 * ql + 2 * j + 1] : -INFINITY;
+                    const float x0 = ((m[q] >> (2 * j)) & 1u) ? s[32 * q + 2 * j] : -INFINITY;
+                    const float x1 = ((m[q] >> (2 * j + 1)) & 1u) ? s[32 * q + 2 * j + 1] : -INFINITY;
                     float e0, e1;
                     f2_unpack(f2_fma(f2_pack(x0, x1), l2e2, neg2), e0, e1);
                     e0 = ex2_approx(e0);
@@ -546,11 +445,11 @@ __device__ __forceinline__ bool masked_probabilities(const float* s, const uint3
 #pragma unroll
                 for (int j = 0; j < 16; ++j) pk[j] = 0u;
             }
-            if (ql == 0) {
-                if (!sy.wait(rh.pv_bar, rh.pv_parity)) return false;
+            if (q == 0) {
+                if (!sy.wait(pv_bar, pv_parity)) return false;
                 tc_fence_after();
             }
-            tmem_st16(rh.p_addr + q * 16, pk);
+            tmem_st16(p_addr + q * 16, pk);
         }
     }
     float a0, a1, b0, b1;
@@ -560,17 +459,101 @@ __device__ __forceinline__ bool masked_probabilities(const float* s, const uint3
     return true;
 }
 
+// Maximum of the masked score row (-inf when the row has no key here).
 template <class C>
-__device__ __forceinline__ float masked_half_max(const float* s, const uint32_t* m, const bool* live) {
+__device__ __forceinline__ float masked_row_max(const float* s, const uint32_t* m, const bool* live) {
     float mx = -INFINITY;
 #pragma unroll
-    for (int ql = 0; ql < C::NWH; ++ql) {
-        if (live[ql]) {
+    for (int q = 0; q < C::NW; ++q) {
+        if (live[q]) {
 #pragma unroll
             for (int b = 0; b < 32; b += 2) {
-                const float x0 = ((m[ql] >> b) & 1u) ? s[32 * ql + b] : -INFINITY;
-                const float x1 = ((m[ql] >> (b + 1)) & 1u) ? s[32 * ql + b + 1] : -INFINITY;
+                const float x0 = ((m[q] >> b) & 1u) ? s[32 * q + b] : -INFINITY;
+                const float x1 = ((m[q] >> (b + 1)) & 1u) ? s[32 * q + b + 1] : -INFINITY;
                 mx = max3f(mx, x0, x1);
+            }
+        }
+    }
+    return mx;
+}
+
+// Byte offset of 16-byte chunk k of row `row` in a K-major operand tile with
+// rows of `rowb` bytes and the matching swizzle (the 16-byte chunk index is
+// XORed with address bits 7.. of the row start, over rowb/16 chunks).
+__device__ __forceinline__ uint32_t swizzled_chunk(int row, int k, int rowb) {
+    return static_cast<uint32_t>(row * rowb + ((k ^ (((row * rowb) >> 7) & (rowb / 16 - 1))) << 4));
+}
+
+// Probabilities for the fast path: chunk row i holds keys [i*CWP, (i+1)*CWP)
+// and is either wholly in this row's H/T window (bit i of rowbits) or not;
+// keys outside the W window already carry -2^40 from the tensor core. The
+// first word is computed before waiting for the previous product.
+template <class C>
+__device__ __forceinline__ bool fast_probabilities(const float* s, uint32_t rowbits, const bool* live,
+                                                   int n_mma, float moff, uint32_t p_addr,
+                                                   const Sync& sy, uint32_t pv_bar,
+                                                   uint32_t pv_parity, float* sum) {
+    const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
+    uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+    for (int q = 0; q < C::NW; ++q) {
+        if (q * 32 < n_mma) {
+            uint32_t pk[16];
+            if (live[q]) {
+#pragma unroll
+                for (int rr = 0; rr < C::RPW; ++rr) {
+                    const int i = q * C::RPW + rr;
+                    const float nm = ((rowbits >> i) & 1u) ? -moff : -INFINITY;
+                    const uint64_t nm2 = f2_pack(nm, nm);
+#pragma unroll
+                    for (int jj = 0; jj < C::CWP / 2; ++jj) {
+                        const int j = rr * (C::CWP / 2) + jj;
+                        float e0, e1;
+                        f2_unpack(f2_fma(f2_pack(s[32 * q + 2 * j], s[32 * q + 2 * j + 1]), l2e2, nm2),
+                                  e0, e1);
+                        e0 = ex2_approx(e0);
+                        e1 = ex2_approx(e1);
+                        pk[j] = pack_bf16x2(e0, e1);
+                        if (j & 1) acc1 = f2_add(acc1, f2_pack(e0, e1));
+                        else acc0 = f2_add(acc0, f2_pack(e0, e1));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) pk[j] = 0u;
+            }
+            if (q == 0) {
+                if (!sy.wait(pv_bar, pv_parity)) return false;
+                tc_fence_after();
+            }
+            tmem_st16(p_addr + q * 16, pk);
+        }
+    }
+    float a0, a1, b0, b1;
+    f2_unpack(acc0, a0, a1);
+    f2_unpack(acc1, b0, b1);
+    *sum = (a0 + a1) + (b0 + b1);
+    return true;
+}
+
+// Maximum over the valid chunk rows (W-masked keys sit at -2^40 and never win:
+// every valid row holds the whole W window of its query).
+template <class C>
+__device__ __forceinline__ float fast_row_max(const float* s, uint32_t rowbits, const bool* live) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < C::NW; ++q) {
+        if (live[q]) {
+#pragma unroll
+            for (int rr = 0; rr < C::RPW; ++rr) {
+                const int i = q * C::RPW + rr;
+                float rm = -INFINITY;
+#pragma unroll
+                for (int jj = 0; jj < C::CWP; jj += 2) {
+                    const int b = 32 * q + rr * C::CWP + jj;
+                    rm = max3f(rm, s[b], s[b + 1]);
+                }
+                mx = ((rowbits >> i) & 1u) ? fmaxf(mx, rm) : mx;
             }
         }
     }
@@ -580,32 +563,16 @@ __device__ __forceinline__ float masked_half_max(const float* s, const uint32_t*
 template <class C>
 __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem,
                              int warp, int lane) {
-    const int quarter = warp & 3, half = warp >> 2;
-    const int r = quarter * 32 + lane;          // tile row = query of the brick = TMEM lane
-    const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int r = warp * 32 + lane;             // tile row = query of the brick = TMEM lane
+    const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const int M = p.bt * p.bh * p.bw;
     const int iw = r % p.bw, ih = (r / p.bw) % p.bh, it = r / (p.bw * p.bh);
-    const int q0 = half * C::NWH;
-    // The two warps sharing these rows meet on their own mbarrier (bounded waits).
-    const uint32_t pair_bar = sy.bar(C::B_PAIR + quarter);
-    uint32_t pair_phase = 0;
-    auto pair_sync = [&]() -> bool {
-        mbar_arrive(pair_bar);
-        const bool ok = sy.wait(pair_bar, pair_phase & 1u);
-        ++pair_phase;
-        return ok;
-    };
-    // exchange slots between the two halves of a row: [parity][half][row]
-    float* xmax = reinterpret_cast<float*>(smem_generic(base + C::OFF_XCH));
-    uint32_t* xflag = reinterpret_cast<uint32_t*>(smem_generic(base + C::OFF_XCH + 2048));
-    float* xsum = reinterpret_cast<float*>(smem_generic(base + C::OFF_XCH + 4096));
     uint32_t g = 0, ul = 0;
 
-    // Qx row of unit `u` (local index `v`), written by the first half: -2^40
-    // where this row's query does not see the chunk column, 0 elsewhere.
+    // Qx row of unit `u` (local index `v`): -2^40 where this row's query does
+    // not see the chunk column, 0 elsewhere; published for the tensor core.
     auto publish_qx = [&](uint32_t v, int u) -> bool {
         if constexpr (C::FAST) {
-            if (half != 0) return true;
             const uint32_t xb = v % C::NQX;
             if (!sy.wait(sy.bar(C::B_XEMPTY + xb), ((v / C::NQX) & 1u) ^ 1u)) return false;
             const Unit X = unit_of(p, u);
@@ -655,12 +622,11 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
                 }
             }
         }
-        float m_ref = -INFINITY;   // reference maximum, log2 units (same in both halves)
-        float l = 0.f;             // this half's running sum of the probabilities
+        float m_ref = -INFINITY;   // reference maximum, log2 units
+        float l = 0.f;             // running sum of the probabilities
         ChunkCursor cur{U.lo_t, 0, 0};
 
         for (int c = 0; c < U.nch; ++c, ++g) {
-            const uint32_t b = g & 1u;
             // chunk geometry for this row (independent of the scores)
             const int kh0 = U.lo_h + cur.hc * p.cr, kw0 = U.lo_w + cur.wc * p.cw;
             const bool t_ok = valid && static_cast<unsigned>(cur.kt - sT) < static_cast<unsigned>(p.KT);
@@ -684,97 +650,84 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
                 }
             }
             cur.advance(U);
+            bool live[C::NW];
+#pragma unroll
+            for (int q = 0; q < C::NW; ++q) {
+                bool mine;
+                if constexpr (C::FAST) mine = (rowbits >> (q * C::RPW)) & ((1u << C::RPW) - 1u);
+                else mine = m[q] != 0u;
+                live[q] = (q * 32 < p.n_mma) && __any_sync(0xffffffffu, mine);
+            }
             bool has_keys;
             if constexpr (C::FAST) has_keys = rowbits != 0u;
             else has_keys = (m[0] | m[1] | m[2] | m[3]) != 0u;
-            uint32_t mh[C::NWH];
-            bool live[C::NWH];
-#pragma unroll
-            for (int ql = 0; ql < C::NWH; ++ql) {
-                const int q = q0 + ql;
-                bool mine;
-                if constexpr (C::FAST) {
-                    mh[ql] = 0u;
-                    mine = (rowbits >> (q * C::RPW)) & ((1u << C::RPW) - 1u);
-                } else {
-                    mh[ql] = half ? m[C::NWH + ql] : m[ql];
-                    mine = mh[ql] != 0u;
-                }
-                live[ql] = (q * 32 < p.n_mma) && __any_sync(0xffffffffu, mine);
-            }
 
-            if (!sy.wait(sy.bar(C::B_SFULL + b), (g >> 1) & 1u)) return;
+            if (!sy.wait(sy.bar(C::B_SFULL), g & 1u)) return;
             tc_fence_after();
-            float s[32 * C::NWH];
+            float s[C::NCAP];
 #pragma unroll
-            for (int ql = 0; ql < C::NWH; ++ql)
-                if ((q0 + ql) * 32 < p.n_mma)
-                    tmem_ld32(t_row + C::TM_S + b * C::NCAP + (q0 + ql) * 32, s + 32 * ql);
+            for (int q = 0; q < C::NW; ++q)
+                if (q * 32 < p.n_mma) tmem_ld32(t_row + C::TM_S + q * 32, s + 32 * q);
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(sy.bar(C::B_SEMPTY + b));   // the tile may take S of chunk g + 2
+            mbar_arrive(sy.bar(C::B_SEMPTY));   // the next score tile may overwrite S now
 
-            // The probability tile b is free once the product of chunk g - 2 is done.
-            const RowHalf rh{q0, p.n_mma, t_row + C::TM_P + b * (C::NCAP / 2),
-                             sy.bar(C::B_PVDONE + b), ((g >> 1) & 1u) ^ 1u};
-            float* xm = xmax + b * 256;
-            uint32_t* xf = xflag + b * 256;
+            // P and O are free once the previous product has completed
+            // (waited for inside the probability writer, after its first word).
+            const uint32_t pv_bar = sy.bar(C::B_PVDONE), pv_parity = (g & 1u) ^ 1u;
 
-            // Reference maximum: exact (both halves' maxima) when a row meets
-            // its first keys; afterwards the kept reference. A chunk whose
-            // probabilities sum past 2^32 in either half (the maximum grew by
-            // ~32 in log2 units) redoes it with the exact maximum. Both halves
-            // of a row take the same decisions (same lanes, same geometry, and
-            // the per-chunk flag exchange). Probabilities keep their relative
-            // precision at any scale, so the result is the same either way.
+            // Fast path: probabilities against the kept reference maximum,
+            // with no max pass. A row meeting its first keys, or a chunk whose
+            // probabilities sum past 2^32 (its maximum grew by ~32 in log2
+            // units), takes the exact path: maximum, rescale, redo.
+            // Probabilities keep their relative precision at any scale, so
+            // both paths give the same result.
+            bool slow = __any_sync(0xffffffffu, has_keys && m_ref == -INFINITY);
+            float lsum = 0.f;
+            if (!slow) {
+                const float moff = m_ref == -INFINITY ? 0.f : m_ref;
+                bool ok;
+                if constexpr (C::FAST)
+                    ok = fast_probabilities<C>(s, rowbits, live, p.n_mma, moff, t_row + C::TM_P, sy,
+                                               pv_bar, pv_parity, &lsum);
+                else
+                    ok = write_probabilities<C>(s, m, live, p.n_mma, moff, t_row + C::TM_P, sy,
+                                                pv_bar, pv_parity, &lsum);
+                if (!ok) return;
+                slow = __any_sync(0xffffffffu, !(lsum <= kSumLimit));
+                if (slow) tmem_wait_st();   // the exact path overwrites this P
+            }
             float alpha = 1.f;
             bool rescale = false;
-            auto exact_max = [&]() -> bool {
+            if (slow) {
                 float mx;
-                if constexpr (C::FAST) mx = fast_half_max<C>(s, rowbits, live, q0);
-                else mx = masked_half_max<C>(s, mh, live);
-                xm[half * 128 + r] = mx;
-                if (!pair_sync()) return false;
-                mx = fmaxf(mx, xm[(half ^ 1) * 128 + r]);
+                if constexpr (C::FAST) mx = fast_row_max<C>(s, rowbits, live);
+                else mx = masked_row_max<C>(s, m, live);
                 const float mx2 = mx * kLog2e;
                 if (mx2 > m_ref + kRescaleThreshold) {
                     if (m_ref != -INFINITY) {
-                        alpha *= ex2_approx(m_ref - mx2);
+                        alpha = ex2_approx(m_ref - mx2);
                         rescale = true;
                     }
                     m_ref = mx2;
                 }
-                return true;
-            };
-            auto probabilities = [&](float* sum) -> bool {
                 const float moff = m_ref == -INFINITY ? 0.f : m_ref;
-                if constexpr (C::FAST) return fast_probabilities<C>(s, rowbits, live, moff, rh, sy, sum);
-                else return masked_probabilities<C>(s, mh, live, moff, rh, sy, sum);
-            };
-
-            if (__any_sync(0xffffffffu, has_keys && m_ref == -INFINITY) && !exact_max()) return;
-            float lsum;
-            if (!probabilities(&lsum)) return;
-            xf[half * 128 + r] = !(lsum <= kSumLimit) ? 1u : 0u;
-            if (!pair_sync()) return;
-            const bool grew = xf[half * 128 + r] | xf[(half ^ 1) * 128 + r];
-            if (__any_sync(0xffffffffu, grew)) {
-                tmem_wait_st();   // the exact redo overwrites this P
-                if (!exact_max()) return;
-                if (!probabilities(&lsum)) return;
-                if (!pair_sync()) return;   // exchange slots are reused next time
+                bool ok;
+                if constexpr (C::FAST)
+                    ok = fast_probabilities<C>(s, rowbits, live, p.n_mma, moff, t_row + C::TM_P, sy,
+                                               pv_bar, pv_parity, &lsum);
+                else
+                    ok = write_probabilities<C>(s, m, live, p.n_mma, moff, t_row + C::TM_P, sy,
+                                                pv_bar, pv_parity, &lsum);
+                if (!ok) return;
             }
             l = l * alpha + lsum;
 
             if (__any_sync(0xffffffffu, rescale)) {
-                // O must hold the product of chunk g - 1 before it is scaled.
-                const uint32_t gp = g - 1;
-                if (!sy.wait(sy.bar(C::B_PVDONE + (gp & 1u)), (gp >> 1) & 1u)) return;
-                tc_fence_after();
                 const float a = rescale ? alpha : 1.f;
 #pragma unroll 1
-                for (int q = half * C::OPH; q < C::OPIECES && q < (half + 1) * C::OPH; ++q) {
-                    float o[32];   // HD = 16 also scales 16 unused columns
+                for (int q = 0; q < C::OPIECES; ++q) {  // HD = 16 also scales 16 unused columns
+                    float o[32];
                     tmem_ld32(t_row + C::TM_O + q * 32, o);
                     tmem_wait_ld();
 #pragma unroll
@@ -784,24 +737,20 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(sy.bar(C::B_PFULL + b));
+            mbar_arrive(sy.bar(C::B_PFULL));
         }
 
         // the next unit's W masks go out before this unit's epilogue
         if (u + static_cast<int>(gridDim.x) < p.n_units && !publish_qx(ul + 1, u + gridDim.x)) return;
 
-        // epilogue: O / l -> bf16 -> global, each half its share of HD
-        xsum[half * 128 + r] = l;
+        // epilogue: O / l -> bf16 -> global
         if (!sy.wait(sy.bar(C::B_OFULL), ul & 1u)) return;
         tc_fence_after();
-        if (!pair_sync()) return;
-        const float lt = l + xsum[(half ^ 1) * 128 + r];
-        if (!pair_sync()) return;
-        const float inv = (valid && lt > 0.f) ? 1.f / lt : 0.f;
+        const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
         const int64_t tok = ((static_cast<int64_t>(U.b) * p.T + t) * p.H + h) * p.W + w;
         uint16_t* orow = p.out + (tok * p.NH + U.n) * C::HD;
 #pragma unroll 1
-        for (int q = half * C::OPH; q < C::OPIECES && q < (half + 1) * C::OPH; ++q) {
+        for (int q = 0; q < C::OPIECES; ++q) {
             float o[32];
             tmem_ld32(t_row + C::TM_O + q * 32, o);
             tmem_wait_ld();
@@ -823,11 +772,11 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
 
 // ------------------------------------------------------------------ kernel
 
-template <int HD, int NCAP, int CWP>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int HD, int NCAP, int NS, int CPS, int CWP>
+__global__ void __launch_bounds__(kThreads, CPS)
 na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
-    using C = Cfg<HD, NCAP, CWP>;
+    using C = Cfg<HD, NCAP, NS, CPS, CWP>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -865,23 +814,19 @@ na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     Sync sy{base + C::OFF_BAR, misc + 1};
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NBAR; ++i) {
-            uint32_t cnt = 1u;
-            if ((i >= C::B_SEMPTY && i < C::B_SEMPTY + 2) || (i >= C::B_PFULL && i < C::B_PFULL + 2) ||
-                i == C::B_OEMPTY)
-                cnt = 256u;   // both softmax warpgroups
-            if (i >= C::B_XFULL && i < C::B_XFULL + C::NQX) cnt = 128u;   // first half only
-            if (i >= C::B_PAIR && i < C::B_PAIR + 4) cnt = 64u;   // the two warps of one row quarter
-            mbar_init(sy.bar(i), cnt);
+            const bool softmax_arrives = i == C::B_SEMPTY || i == C::B_PFULL || i == C::B_OEMPTY ||
+                                         (i >= C::B_XFULL && i < C::B_XFULL + C::NQX);
+            mbar_init(sy.bar(i), softmax_arrives ? 128u : 1u);
         }
         misc[1] = 0u;
         fence_mbar_init();
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == 4 && lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
     }
-    if (warp == 9) {
+    if (warp == 5) {
         tmem_alloc(base + C::OFF_MISC, C::TM_COLS);
         tmem_relinquish();
     }
@@ -890,19 +835,19 @@ na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = misc[0];
 
-    if (warp < 8) {
-        regs_increase<C::REGS_HIGH>();
+    if (warp < 4) {
+        if (C::CPS == 2) regs_increase<C::REGS_HIGH>();
         softmax_role<C>(p, sy, base, tmem, warp, lane);
     } else {
-        regs_decrease<C::REGS_LOW>();
-        if (warp == 8 && lane == 0) producer_role<C>(p, &tm_q, &tm_k, &tm_v, sy, base);
-        if (warp == 9 && lane == 0) mma_s_role<C>(p, sy, base, tmem);
-        if (warp == 10 && lane == 0) mma_pv_role<C>(p, sy, base, tmem);
+        if (C::CPS == 2) regs_decrease<C::REGS_LOW>();
+        if (warp == 4 && lane == 0) producer_role<C>(p, &tm_q, &tm_k, &tm_v, sy, base);
+        if (warp == 5 && lane == 0) mma_s_role<C>(p, sy, base, tmem);
+        if (warp == 6 && lane == 0) mma_pv_role<C>(p, sy, base, tmem);
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TM_COLS);
     }
@@ -910,11 +855,11 @@ na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
 // ------------------------------------------------------------------ host side
 
-template <int HD, int NCAP, int CWP>
+template <int HD, int NCAP, int NS, int CPS, int CWP>
 static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const KernelParams& kp, int grid, cudaStream_t stream) {
-    using C = Cfg<HD, NCAP, CWP>;
-    auto kern = na3d_fwd_sm103<HD, NCAP, CWP>;
+    using C = Cfg<HD, NCAP, NS, CPS, CWP>;
+    auto kern = na3d_fwd_sm103<HD, NCAP, NS, CPS, CWP>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
@@ -922,32 +867,32 @@ static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const 
     return cudaGetLastError();
 }
 
-template <int HD, int NCAP, int CWP>
+template <int HD, int NCAP, int NS, int CPS, int CWP>
 static void info_t(VariantInfo* v) {
-    using C = Cfg<HD, NCAP, CWP>;
+    using C = Cfg<HD, NCAP, NS, CPS, CWP>;
     v->ncap = NCAP;
-    v->stages = C::NS;
+    v->stages = NS;
     v->hd_box = C::HDB;
     v->smem = C::SMEM_ALLOC;
-    v->ctas_per_sm = 1;
+    v->ctas_per_sm = CPS;
 }
 
-// The instance table: (HD, score-tile cap) x chunk stride CWP (0: generic
-// per-key masks; 8, 16, 32: W window applied by the tensor core).
+// The instance table: (HD, score-tile cap, K/V stages, CTAs per SM) x chunk
+// stride CWP (0: generic masks; 8, 16, 32: W window applied by the tensor core).
 #define NA3D_HD_TABLE(X, CWP) \
-    X(16, 128, CWP)           \
-    X(32, 128, CWP)           \
-    X(64, 128, CWP)           \
-    X(128, 128, CWP)          \
-    X(256, 64, CWP)
+    X(16, 128, 4, 2, CWP)     \
+    X(32, 128, 3, 2, CWP)     \
+    X(64, 128, 2, 2, CWP)     \
+    X(128, 64, 2, 2, CWP)     \
+    X(256, 64, 2, 1, CWP)
 #define NA3D_VARIANTS(X) \
     NA3D_HD_TABLE(X, 0) NA3D_HD_TABLE(X, 8) NA3D_HD_TABLE(X, 16) NA3D_HD_TABLE(X, 32)
 
 bool variant_info(int hd, int cwp, VariantInfo* info) {
-#define X(hd_, n_, w_)                     \
-    if (hd == hd_ && cwp == w_) {          \
-        info_t<hd_, n_, w_>(info);         \
-        return true;                       \
+#define X(hd_, n_, s_, c_, w_)                   \
+    if (hd == hd_ && cwp == w_) {                \
+        info_t<hd_, n_, s_, c_, w_>(info);       \
+        return true;                             \
     }
     NA3D_VARIANTS(X)
 #undef X
@@ -957,8 +902,8 @@ bool variant_info(int hd, int cwp, VariantInfo* info) {
 cudaError_t launch_fwd(int hd, int cwp, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const KernelParams& kp, int grid,
                        cudaStream_t stream) {
-#define X(hd_, n_, w_) \
-    if (hd == hd_ && cwp == w_) return launch_t<hd_, n_, w_>(tq, tk, tv, kp, grid, stream);
+#define X(hd_, n_, s_, c_, w_) \
+    if (hd == hd_ && cwp == w_) return launch_t<hd_, n_, s_, c_, w_>(tq, tk, tv, kp, grid, stream);
     NA3D_VARIANTS(X)
 #undef X
     return cudaErrorInvalidValue;
