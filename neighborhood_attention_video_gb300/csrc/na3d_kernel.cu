@@ -627,6 +627,13 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
         ChunkCursor cur{U.lo_t, 0, 0};
 
         for (int c = 0; c < U.nch; ++c, ++g) {
+            if (!sy.wait(sy.bar(C::B_SFULL), g & 1u)) return;
+            tc_fence_after();
+            float s[C::NCAP];   // loaded asynchronously; not read before tmem_wait_ld
+#pragma unroll
+            for (int q = 0; q < C::NW; ++q)
+                if (q * 32 < p.n_mma) tmem_ld32(t_row + C::TM_S + q * 32, s + 32 * q);
+            // The window mask of this chunk is built while the score loads are in flight.
             // chunk geometry for this row (independent of the scores)
             const int kh0 = U.lo_h + cur.hc * p.cr, kw0 = U.lo_w + cur.wc * p.cw;
             const bool t_ok = valid && static_cast<unsigned>(cur.kt - sT) < static_cast<unsigned>(p.KT);
@@ -662,12 +669,6 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
             if constexpr (C::FAST) has_keys = rowbits != 0u;
             else has_keys = (m[0] | m[1] | m[2] | m[3]) != 0u;
 
-            if (!sy.wait(sy.bar(C::B_SFULL), g & 1u)) return;
-            tc_fence_after();
-            float s[C::NCAP];
-#pragma unroll
-            for (int q = 0; q < C::NW; ++q)
-                if (q * 32 < p.n_mma) tmem_ld32(t_row + C::TM_S + q * 32, s + 32 * q);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(sy.bar(C::B_SEMPTY));   // the next score tile may overwrite S now
