@@ -75,6 +75,28 @@ int na3d_fwd(const void* q, const void* k, const void* v, void* out,
              int64_t B, int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD,
              int64_t KT, int64_t KH, int64_t KW, void* stream);
 
+/*
+ * na3d_fwd_strided - na3d_fwd for inputs whose grid positions are not packed:
+ * q, k and v each hold, for token p = ((b*T + t)*H + h)*W + w, its NH heads
+ * of HD values at  base + p*token_stride + head*HD  (elements). This is the
+ * layout of a fused QKV projection output [B,T,H,W,3,NH,HD]: token_stride =
+ * 3*NH*HD, with q, k, v pointing at the three blocks of the first token, so
+ * the projection output feeds the attention without a gather copy (the
+ * copy the pages' benchmark pays: "[Triton/Gluon] Add 3D neighborhood flash
+ * attention (na3d_flash)", Performance table, "times include the wrapper's
+ * v.contiguous() staging copy").
+ *
+ * q_token_stride, k_token_stride, v_token_stride: >= NH*HD, in elements; a
+ * stride times 2 bytes must be a multiple of 16. out stays contiguous
+ * (B,T,H,W,NH,HD) and must not overlap the memory spanned by q, k or v.
+ * All other arguments, the errors and the asynchrony are those of na3d_fwd;
+ * a bad stride returns NA3D_ERR_SHAPE (too small) or NA3D_ERR_ALIGN.
+ */
+int na3d_fwd_strided(const void* q, const void* k, const void* v, void* out,
+                     int64_t B, int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD,
+                     int64_t KT, int64_t KH, int64_t KW, int64_t q_token_stride,
+                     int64_t k_token_stride, int64_t v_token_stride, void* stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* na3d_status_string(int status);
 

@@ -13,13 +13,14 @@ import ctypes
 import os
 
 __all__ = [
-    "NA3DError", "NA3DUnavailable", "na3d_fwd", "na3d_status_string", "na3d_plan",
+    "NA3DError", "NA3DUnavailable", "na3d_fwd", "na3d_fwd_strided", "na3d_status_string", "na3d_plan",
     "na3d_device_status", "library_path", "load_library", "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libna3d.so")
-EXPORTED_SYMBOLS = ("na3d_fwd", "na3d_status_string", "na3d_plan", "na3d_device_status")
+EXPORTED_SYMBOLS = ("na3d_fwd", "na3d_fwd_strided", "na3d_status_string", "na3d_plan",
+                    "na3d_device_status")
 
 NA3D_OK = 0
 _I64 = ctypes.c_int64
@@ -63,6 +64,8 @@ def load_library():
     lib = ctypes.CDLL(LIB_PATH)
     lib.na3d_fwd.argtypes = [_P, _P, _P, _P] + [_I64] * 9 + [_P]
     lib.na3d_fwd.restype = ctypes.c_int
+    lib.na3d_fwd_strided.argtypes = [_P, _P, _P, _P] + [_I64] * 12 + [_P]
+    lib.na3d_fwd_strided.restype = ctypes.c_int
     lib.na3d_status_string.argtypes = [ctypes.c_int]
     lib.na3d_status_string.restype = ctypes.c_char_p
     lib.na3d_plan.argtypes = [_I64] * 8 + [ctypes.POINTER(PlanInfo)]
@@ -109,6 +112,43 @@ def na3d_fwd(q, k, v, out, kernel_size, stream=None) -> None:
                       *[int(x) for x in q.shape], KT, KH, KW, _stream_handle(stream))
     if rc != NA3D_OK:
         raise NA3DError(rc, "na3d_fwd")
+
+
+def _token_stride(name, t) -> int:
+    """Elements between consecutive (b,t,h,w) positions of a (B,T,H,W,NH,HD)
+    view whose heads are packed (head stride HD, unit element stride)."""
+    st, sh = t.stride(), t.shape
+    if st[5] != 1 or (sh[4] > 1 and st[4] != sh[5]):
+        raise ValueError(f"{name}: heads must be packed (strides [..., HD, 1])")
+    for i in (2, 1, 0):
+        if sh[i] > 1 and st[i] != sh[i + 1] * st[i + 1]:
+            raise ValueError(f"{name}: grid positions must share one token stride")
+    return int(st[3])
+
+
+def na3d_fwd_strided(q, k, v, out, kernel_size, stream=None) -> None:
+    """``na3d_fwd`` for q, k, v views with a token stride, e.g. the three
+    slices ``x[..., 0, :, :]``, ``x[..., 1, :, :]``, ``x[..., 2, :, :]`` of a
+    fused projection output ``x`` of shape (B, T, H, W, 3, NH, HD). ``out`` is
+    a contiguous (B, T, H, W, NH, HD) bf16 CUDA tensor."""
+    import torch
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a bfloat16 CUDA tensor")
+        if t.dim() != 6 or tuple(t.shape) != tuple(q.shape):
+            raise ValueError("q, k, v and out must have the same 6-D shape")
+    if not out.is_contiguous():
+        raise ValueError("out must be contiguous")
+    strides = [_token_stride(n, t) for n, t in (("q", q), ("k", k), ("v", v))]
+    KT, KH, KW = (int(x) for x in kernel_size)
+    rc = lib.na3d_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              *[int(x) for x in q.shape], KT, KH, KW, *strides,
+                              _stream_handle(stream))
+    if rc != NA3D_OK:
+        raise NA3DError(rc, "na3d_fwd_strided")
 
 
 def na3d_plan(T, H, W, NH, HD, KT, KH, KW) -> dict:

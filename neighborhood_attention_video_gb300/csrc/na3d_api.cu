@@ -164,15 +164,16 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// The (B,T,H,W,NH,HD) tensor viewed as 5-D (NH*HD, W, H, T, B): a box of
+// The (B,T,H,W,NH,HD) tensor viewed as 5-D (NH*HD, W, H, T, B), with
+// `token_stride` elements between consecutive grid positions: a box of
 // {hd_box, bx, by, bz, 1} at x = head*HD + column picks one head's rows.
 bool encode_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t H, int64_t W,
-                int64_t NH, int64_t HD, int hd_box, int bx, int by, int bz) {
+                int64_t NH, int64_t HD, int64_t token_stride, int hd_box, int bx, int by, int bz) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[5] = {cuuint64_t(NH * HD), cuuint64_t(W), cuuint64_t(H), cuuint64_t(T),
                                 cuuint64_t(B)};
-    const cuuint64_t row = cuuint64_t(NH * HD * 2);
+    const cuuint64_t row = cuuint64_t(token_stride * 2);
     const cuuint64_t strides[4] = {row, row * W, row * W * H, row * W * H * T};
     const cuuint32_t box[5] = {cuuint32_t(hd_box), cuuint32_t(bx), cuuint32_t(by), cuuint32_t(bz), 1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
@@ -184,9 +185,10 @@ bool encode_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t H
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool overlaps(const void* a, const void* b, int64_t bytes) {
+// Do the byte ranges [a, a + a_bytes) and [b, b + b_bytes) intersect?
+bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-    return x < y + uintptr_t(bytes) && y < x + uintptr_t(bytes);
+    return x < y + uintptr_t(b_bytes) && y < x + uintptr_t(a_bytes);
 }
 
 }  // namespace
@@ -230,18 +232,31 @@ int na3d_plan(int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t K
     return NA3D_OK;
 }
 
-int na3d_fwd(const void* q, const void* k, const void* v, void* out, int64_t B, int64_t T,
-             int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT, int64_t KH, int64_t KW,
-             void* stream) {
+int na3d_fwd_strided(const void* q, const void* k, const void* v, void* out, int64_t B, int64_t T,
+                     int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT, int64_t KH,
+                     int64_t KW, int64_t q_token_stride, int64_t k_token_stride,
+                     int64_t v_token_stride, void* stream) {
     int rc = validate_shape(B, T, H, W, NH, HD, KT, KH, KW);
     if (rc != NA3D_OK) return rc;
     const int64_t bytes = B * T * H * W * NH * HD * 2;
     if (bytes == 0) return NA3D_OK;  // B == 0 or NH == 0: nothing to read or write
     if (!q || !k || !v || !out) return NA3D_ERR_NULL;
+    const int64_t strides[3] = {q_token_stride, k_token_stride, v_token_stride};
+    int64_t spans[3];
+    const int64_t tokens = B * T * H * W;
+    for (int i = 0; i < 3; ++i) {
+        if (strides[i] < NH * HD) return NA3D_ERR_SHAPE;
+        if ((strides[i] * 2) % 16 != 0) return NA3D_ERR_ALIGN;
+        int64_t span;
+        if (!mul_ok(tokens - 1, strides[i], &span) || !mul_ok(span + NH * HD, 2, &spans[i]) ||
+            strides[i] * 2 >= (int64_t(1) << 40) / (W * H * T > 0 ? W * H * T : 1))
+            return NA3D_ERR_OVERFLOW;
+    }
     const void* ptrs[4] = {q, k, v, out};
     for (const void* p : ptrs)
         if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return NA3D_ERR_ALIGN;
-    if (overlaps(out, q, bytes) || overlaps(out, k, bytes) || overlaps(out, v, bytes))
+    if (overlaps(out, bytes, q, spans[0]) || overlaps(out, bytes, k, spans[1]) ||
+        overlaps(out, bytes, v, spans[2]))
         return NA3D_ERR_ALIAS;
 
     int dev = 0, major = 0, minor = 0, sms = 0;
@@ -275,9 +290,9 @@ int na3d_fwd(const void* q, const void* k, const void* v, void* out, int64_t B, 
     kp.div_nbt = na3d::make_fastdiv(kp.nbt);
 
     CUtensorMap tq, tk, tv;
-    if (!encode_map(&tq, q, B, T, H, W, NH, HD, vi.hd_box, pl.bw, pl.bh, pl.bt) ||
-        !encode_map(&tk, k, B, T, H, W, NH, HD, vi.hd_box, pl.cw, pl.cr, 1) ||
-        !encode_map(&tv, v, B, T, H, W, NH, HD, vi.hd_box, pl.cw, pl.cr, 1))
+    if (!encode_map(&tq, q, B, T, H, W, NH, HD, q_token_stride, vi.hd_box, pl.bw, pl.bh, pl.bt) ||
+        !encode_map(&tk, k, B, T, H, W, NH, HD, k_token_stride, vi.hd_box, pl.cw, pl.cr, 1) ||
+        !encode_map(&tv, v, B, T, H, W, NH, HD, v_token_stride, vi.hd_box, pl.cw, pl.cr, 1))
         return NA3D_ERR_CUDA;
 
     const int64_t slots = int64_t(sms) * vi.ctas_per_sm;   // persistent CTAs
@@ -286,6 +301,13 @@ int na3d_fwd(const void* q, const void* k, const void* v, void* out, int64_t B, 
         cudaSuccess)
         return NA3D_ERR_CUDA;
     return NA3D_OK;
+}
+
+int na3d_fwd(const void* q, const void* k, const void* v, void* out, int64_t B, int64_t T,
+             int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT, int64_t KH, int64_t KW,
+             void* stream) {
+    return na3d_fwd_strided(q, k, v, out, B, T, H, W, NH, HD, KT, KH, KW, NH * HD, NH * HD,
+                            NH * HD, stream);
 }
 
 int na3d_device_status(void* stream) {

@@ -199,3 +199,24 @@ def test_output_untouched_outside_the_tensor():
     torch.cuda.synchronize()
     assert bool((buf[:guard] == 7.0).all()) and bool((buf[guard + n:] == 7.0).all())
     check(from_dev(out.contiguous()), oracle.na3d_fwd(q, k, v, kernel), "guarded")
+
+
+# ------------------------------------------------------------ strided (fused QKV) inputs
+
+@pytest.mark.parametrize("shape,kernel", [((1, 6, 20, 36, 2, 64), (3, 7, 7)),
+                                          ((2, 5, 13, 19, 3, 128), (3, 5, 7)),
+                                          ((1, 8, 24, 33, 2, 64), (3, 7, 33))],
+                         ids=lambda x: "x".join(map(str, x)))
+def test_fused_qkv_views_match_contiguous(shape, kernel):
+    """q, k, v as the three slices of one fused [B,T,H,W,3,NH,HD] projection
+    output: same result as contiguous inputs, and parity with the oracle."""
+    B, T, H, W, NH, HD = shape
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=6)
+    fused = np.stack([q, k, v], axis=4)          # (B, T, H, W, 3, NH, HD)
+    fd = torch.from_numpy(fused.view(np.int16)).cuda().view(torch.bfloat16)
+    out = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    na.na3d_fwd_strided(fd[:, :, :, :, 0], fd[:, :, :, :, 1], fd[:, :, :, :, 2], out, kernel)
+    torch.cuda.synchronize()
+    got = from_dev(out)
+    np.testing.assert_array_equal(got, run_gpu(q, k, v, kernel))
+    check(got, oracle.na3d_fwd(q, k, v, kernel), f"fused {shape} {kernel}")

@@ -83,6 +83,27 @@ def test_pointer_validation(lib):
     assert call_fwd(lib, (base, base, base, base + n_bytes)) not in (ERR_ALIAS, ERR_NULL, ERR_ALIGN)
 
 
+def call_strided(lib, ptrs, strides, dims=(1, 4, 8, 16, 2, 32), kernel=(3, 5, 5)):
+    return lib.na3d_fwd_strided(*[ctypes.c_void_p(p) for p in ptrs], *dims, *kernel, *strides, None)
+
+
+def test_strided_validation(lib):
+    nhd = 2 * 32
+    base = 1 << 20
+    ok = (base, base + 2 * nhd, base + 4 * nhd, 1 << 30)
+    # a fused [.., 3, NH, HD] layout passes validation (fails later only for want of a GPU)
+    import torch
+    expect = OK if torch.cuda.is_available() else ERR_CUDA
+    assert call_strided(lib, ok, (3 * nhd, 3 * nhd, 3 * nhd)) == expect
+    assert call_strided(lib, ok, (nhd - 8, 3 * nhd, 3 * nhd)) == ERR_SHAPE
+    assert call_strided(lib, ok, (3 * nhd + 4, 3 * nhd, 3 * nhd)) == ERR_ALIGN
+    # out overlapping the strided span of v
+    n_tokens = 4 * 8 * 16
+    inside_v = base + 4 * nhd + 2 * (3 * nhd) * (n_tokens // 2)
+    assert call_strided(lib, (base, base + 2 * nhd, base + 4 * nhd, inside_v - inside_v % 16),
+                        (3 * nhd,) * 3) == ERR_ALIAS
+
+
 def test_empty_problem_is_a_no_op(lib):
     assert call_fwd(lib, (16, 32, 48, 64), dims=(0, 4, 8, 16, 2, 32)) == OK
     assert call_fwd(lib, (16, 32, 48, 64), dims=(1, 4, 8, 16, 0, 32)) == OK
