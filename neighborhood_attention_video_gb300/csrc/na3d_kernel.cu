@@ -27,10 +27,15 @@
 //   warp 6      product issuer: O += P V with P read from tensor memory.
 //   warp 7      idle (it completes warpgroup 1 for the register hand-over).
 //
-// Tensor memory per CTA: S (NCAP fp32 columns), P (NCAP/2 columns of bf16
-// pairs) and O (HD columns). S is free again as soon as the softmax has read
-// it into registers, so the next score tile is computed while the softmax
-// works on the current one.
+// Tensor memory per CTA: O (HD fp32 columns) and a ring of NSLOT slots of
+// NCAP/2 columns. A score tile S (NCAP fp32 columns) takes two consecutive
+// slots; once the softmax has read it into registers, it writes P (NCAP/2
+// columns of bf16 pairs) over the first of them and the second is free. So the
+// next score tile is computed while the softmax works on the current one, and
+// the softmax never waits for the previous product: P(g) and P(g-1) sit in
+// different slots. A score tile waits only for the product that last read its
+// slots, LAG chunks back. With three slots the ring wraps every third chunk;
+// that tile is issued as two halves.
 //
 // Every pipeline wait is bounded: a wait that runs out sets a device flag, all
 // roles drop out of their loops, in-flight copies and MMAs are drained, and
@@ -83,6 +88,21 @@ struct Cfg {
     static constexpr int KV_TILE = NREG * KV_REG;
     static constexpr int NW = NCAP / 32;            // 32-column words per score row
     static constexpr int OPIECES = (HD + 31) / 32;  // 32-column TMEM loads per output row
+    static constexpr uint32_t TM_COLS = CPS == 2 ? 256 : 512;
+    static constexpr uint32_t TM_O = 0;                              // HD fp32 output columns
+    static constexpr uint32_t OCOLS = OPIECES * 32 < 64 ? 64 : OPIECES * 32;
+    static constexpr uint32_t SW = NCAP / 2;                         // slot width = P columns
+    static constexpr uint32_t TM_R = OCOLS;                          // first ring column
+    static constexpr int NSLOT = static_cast<int>((TM_COLS - OCOLS) / SW);
+    static constexpr int STEP = NSLOT % 2 == 0 ? 2 : 1;   // slots a chunk advances the ring by
+    static constexpr int RING = NSLOT / STEP;             // distinct P slots in rotation
+    static constexpr int LAG = STEP == 1 ? NSLOT - 1 : RING;   // S(g) reuses P(g - LAG)'s slot
+    // S(g) overwrites columns of S(g - SLAG): with pairs of slots (STEP 2) the
+    // next tile goes to other columns and is issued before the softmax has
+    // read the current one
+    static constexpr int SLAG = STEP == 1 ? 1 : RING;
+    // first slot of chunk g's score tile (and of its P)
+    static __device__ __forceinline__ uint32_t slot_of(uint32_t g) { return (g * STEP) % NSLOT; }
     // Shared memory: double-buffer Q and Qx where the per-SM share allows it.
     static constexpr int LIMIT = (CPS == 2 ? 115712 : 232448) - 1024 - 512;
     static constexpr int FIXED = 2 * NS * KV_TILE + (FAST ? KX_TILE : 0);
@@ -99,25 +119,27 @@ struct Cfg {
     static constexpr int B_KFULL = 2 * NQ, B_KEMPTY = B_KFULL + NS;
     static constexpr int B_VFULL = B_KEMPTY + NS, B_VEMPTY = B_VFULL + NS;
     static constexpr int B_XFULL = B_VEMPTY + NS, B_XEMPTY = B_XFULL + NQX;
-    static constexpr int B_SFULL = B_XEMPTY + NQX, B_SEMPTY = B_SFULL + 1, B_PFULL = B_SFULL + 2,
-                         B_PVDONE = B_SFULL + 3, B_OFULL = B_SFULL + 4, B_OEMPTY = B_SFULL + 5,
-                         B_DRAIN = B_SFULL + 6, B_DRAIN2 = B_SFULL + 7, NBAR = B_SFULL + 8;
+    // For chunk c: S(c) ready, S(c) read, P(c) written and the product of c
+    // done are signalled on B_SFULL, B_SEMPTY, B_PFULL and B_PFREE + c % RING:
+    // one barrier per ring position, so a softmax warp that runs ahead of the
+    // others never completes another chunk's phase, and no waiter ever sees a
+    // phase alias (the next use of a barrier needs the current one consumed).
+    static constexpr int B_OFULL = B_XEMPTY + NQX, B_OEMPTY = B_OFULL + 1, B_DRAIN = B_OFULL + 2,
+                         B_DRAIN2 = B_OFULL + 3, B_SFULL = B_OFULL + 4, B_SEMPTY = B_SFULL + RING,
+                         B_PFULL = B_SEMPTY + RING, B_PFREE = B_PFULL + RING, NBAR = B_PFREE + RING;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
     // The floor keeps the CTA count per SM at CPS (tensor memory is sized for it).
     static constexpr int MIN_SMEM = CPS == 2 ? 80 * 1024 : 120 * 1024;
     static constexpr int SMEM_ALLOC = (SMEM_USED + 1024) > MIN_SMEM ? (SMEM_USED + 1024) : MIN_SMEM;
-    static constexpr uint32_t TM_S = 0;                    // NCAP fp32 score columns
-    static constexpr uint32_t TM_P = NCAP;                 // NCAP / 2 columns of bf16 pairs
-    static constexpr uint32_t TM_O = NCAP + NCAP / 2;      // HD fp32 output columns
-    static constexpr uint32_t TM_NEED = TM_O + OPIECES * 32;
-    static constexpr uint32_t TM_COLS = TM_NEED <= 256 ? 256 : 512;
     // registers: warpgroup 1 gives its share to the softmax warpgroup
     static constexpr uint32_t REGS_LAUNCH = 65536 / (kThreads * CPS) >= 256 ? 255 : 65536 / (kThreads * CPS);
     static constexpr uint32_t REGS_LOW = 56;
     static constexpr uint32_t REGS_HIGH = CPS == 2 ? 200 : 232;
     static_assert(CPS == 1 || (REGS_HIGH + REGS_LOW) * 128 <= REGS_LAUNCH * kThreads, "register split");
     static_assert(TM_COLS * CPS <= 512, "TMEM budget");
+    static_assert(NSLOT >= 3 && TM_R + NSLOT * SW <= TM_COLS && OPIECES * 32 <= OCOLS, "TMEM ring");
+    static_assert(LAG <= RING, "a product barrier never runs a phase ahead of its waiter");
     static_assert(SMEM_ALLOC * CPS <= 232448 && SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(NCAP == 64 || NCAP == 128, "score tile width");
     static_assert(NS >= 2, "K/V rings need two stages");
@@ -319,8 +341,12 @@ struct ChunkWalk {
 // other's issue and sit on different SM sub-partitions.
 template <class C>
 __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem) {
+    // a tile that wraps around the ring is issued as two halves of SW keys
+    const int n_lo = p.n_mma < static_cast<int>(C::SW) ? p.n_mma : static_cast<int>(C::SW);
+    const int n_hi = p.n_mma - n_lo;
     const uint32_t idesc_s = make_idesc_bf16(128, p.n_mma, 0, 0);
-    const uint32_t d_s = tmem + C::TM_S;
+    const uint32_t idesc_lo = make_idesc_bf16(128, n_lo, 0, 0);
+    const uint32_t idesc_hi = n_hi > 0 ? make_idesc_bf16(128, n_hi, 0, 0) : 0u;
     const uint64_t qd0 = make_smem_desc(base + C::OFF_Q, 16, C::SBO, C::SWZ);
     const uint64_t kd0 = make_smem_desc(base + C::OFF_K, 16, C::SBO, C::SWZ);
     const uint32_t q_hi = static_cast<uint32_t>(qd0 >> 32), k_hi = static_cast<uint32_t>(kd0 >> 32);
@@ -332,6 +358,24 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
         x_lo0 = static_cast<uint32_t>(xd0);
         y_lo = static_cast<uint32_t>(yd0);
     }
+    // S = Q K^T + Qx Kx^T for the keys whose K and Kx rows start at k_lo and
+    // y_l, into TMEM column d
+    auto issue = [&](uint32_t d, uint32_t q_lo, uint32_t k_lo, uint32_t x_lo, uint32_t y_l,
+                     uint32_t idesc) {
+#pragma unroll
+        for (int kk = 0; kk < C::HD / 16; ++kk) {
+            constexpr int kPer = C::HDB / 16;   // k-steps per swizzle row
+            const uint32_t qo = ((kk / kPer) * C::Q_REG + (kk % kPer) * 32) >> 4;
+            const uint32_t ko = ((kk / kPer) * C::KV_REG + (kk % kPer) * 32) >> 4;
+            if (kk == 0) umma_ss_halves<0>(d, q_lo + qo, q_hi, k_lo + ko, k_hi, idesc);
+            else umma_ss_halves<1>(d, q_lo + qo, q_hi, k_lo + ko, k_hi, idesc);
+        }
+        if constexpr (C::FAST) {   // -2^40 on keys outside each row's W window
+#pragma unroll
+            for (int kk = 0; kk < C::KEXT / 16; ++kk)
+                umma_ss_halves<1>(d, x_lo + kk * 2, x_hi, y_l + kk * 2, x_hi, idesc);
+        }
+    };
     ChunkWalk w;
     w.start(p);
     while (!w.done(p)) {
@@ -343,25 +387,31 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
             if (w.c == 0 && !sy.wait(sy.bar(C::B_XFULL + xb), (w.ul / C::NQX) & 1u)) break;
         }
         if (!sy.wait(sy.bar(C::B_KFULL + st), (w.g / C::NS) & 1u)) break;
-        if (!sy.wait(sy.bar(C::B_SEMPTY), (w.g & 1u) ^ 1u)) break;
+        // the tile that last used these columns has been read, and the
+        // product that last read them has completed
+        if (w.g >= static_cast<uint32_t>(C::SLAG)) {
+            const uint32_t sc = w.g - C::SLAG;
+            if (!sy.wait(sy.bar(C::B_SEMPTY + sc % C::RING), (sc / C::RING) & 1u)) break;
+        }
+        if (w.g >= static_cast<uint32_t>(C::LAG)) {
+            const uint32_t pc = w.g - C::LAG;
+            if (!sy.wait(sy.bar(C::B_PFREE + pc % C::RING), (pc / C::RING) & 1u)) break;
+        }
         tc_fence_after();
         const uint32_t q_lo = static_cast<uint32_t>(qd0) + ((qb * C::Q_TILE) >> 4);
         const uint32_t k_lo = static_cast<uint32_t>(kd0) + ((st * C::KV_TILE) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < C::HD / 16; ++kk) {
-            constexpr int kPer = C::HDB / 16;   // k-steps per swizzle row
-            const uint32_t qo = ((kk / kPer) * C::Q_REG + (kk % kPer) * 32) >> 4;
-            const uint32_t ko = ((kk / kPer) * C::KV_REG + (kk % kPer) * 32) >> 4;
-            if (kk == 0) umma_ss_halves<0>(d_s, q_lo + qo, q_hi, k_lo + ko, k_hi, idesc_s);
-            else umma_ss_halves<1>(d_s, q_lo + qo, q_hi, k_lo + ko, k_hi, idesc_s);
+        const uint32_t x_lo = C::FAST ? x_lo0 + ((xb * C::QX_TILE) >> 4) : 0u;
+        const uint32_t slot = C::slot_of(w.g);
+        const uint32_t d = tmem + C::TM_R + slot * C::SW;
+        if (C::STEP == 1 && slot + 1 == static_cast<uint32_t>(C::NSLOT)) {
+            issue(d, q_lo, k_lo, x_lo, y_lo, idesc_lo);
+            if (n_hi > 0)   // keys SW.. go to the first slot of the ring
+                issue(tmem + C::TM_R, q_lo, k_lo + ((C::SW * C::ROWB) >> 4), x_lo,
+                      y_lo + ((C::SW * C::XROWB) >> 4), idesc_hi);
+        } else {
+            issue(d, q_lo, k_lo, x_lo, y_lo, idesc_s);
         }
-        if constexpr (C::FAST) {   // S += Qx Kx^T: -2^40 on keys outside each row's W window
-            const uint32_t x_lo = x_lo0 + ((xb * C::QX_TILE) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < C::KEXT / 16; ++kk)
-                umma_ss_halves<1>(d_s, x_lo + kk * 2, x_hi, y_lo + kk * 2, x_hi, idesc_s);
-        }
-        umma_commit(sy.bar(C::B_SFULL));
+        umma_commit(sy.bar(C::B_SFULL + w.g % C::RING));
         umma_commit(sy.bar(C::B_KEMPTY + st));
         if (w.c == w.nch - 1) {
             umma_commit(sy.bar(C::B_QEMPTY + qb));
@@ -379,7 +429,7 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
 template <class C>
 __device__ void mma_pv_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem) {
     const uint32_t idesc_o = make_idesc_bf16(128, C::HD, 0, 1);
-    const uint32_t d_o = tmem + C::TM_O, a_p = tmem + C::TM_P;
+    const uint32_t d_o = tmem + C::TM_O;
     const uint64_t vd0 = make_smem_desc(base + C::OFF_V, C::KV_REG, C::SBO, C::SWZ);
     const uint32_t v_hi = static_cast<uint32_t>(vd0 >> 32);
     const int ksteps = p.n_mma >> 4;
@@ -389,16 +439,17 @@ __device__ void mma_pv_role(const KernelParams& p, const Sync& sy, uint32_t base
         const uint32_t st = w.g % C::NS;
         if (w.c == 0 && !sy.wait(sy.bar(C::B_OEMPTY), (w.ul & 1u) ^ 1u)) break;
         if (!sy.wait(sy.bar(C::B_VFULL + st), (w.g / C::NS) & 1u)) break;
-        if (!sy.wait(sy.bar(C::B_PFULL), w.g & 1u)) break;
+        if (!sy.wait(sy.bar(C::B_PFULL + w.g % C::RING), (w.g / C::RING) & 1u)) break;
         tc_fence_after();
         const uint32_t v_lo = static_cast<uint32_t>(vd0) + ((st * C::KV_TILE) >> 4);
+        const uint32_t a_p = tmem + C::TM_R + C::slot_of(w.g) * C::SW;
         if (w.c == 0) umma_ts_halves<0>(d_o, a_p, v_lo, v_hi, idesc_o);
         else umma_ts_halves<1>(d_o, a_p, v_lo, v_hi, idesc_o);
 #pragma unroll
         for (int kk = 1; kk < C::NCAP / 16; ++kk)
             if (kk < ksteps)
                 umma_ts_halves<1>(d_o, a_p + kk * 8, v_lo + ((kk * 16 * C::ROWB) >> 4), v_hi, idesc_o);
-        umma_commit(sy.bar(C::B_PVDONE));
+        umma_commit(sy.bar(C::B_PFREE + w.g % C::RING));
         umma_commit(sy.bar(C::B_VEMPTY + st));
         if (w.c == w.nch - 1) umma_commit(sy.bar(C::B_OFULL));
         w.next(p);
@@ -411,16 +462,10 @@ __device__ void mma_pv_role(const KernelParams& p, const Sync& sy, uint32_t base
 
 // P = 2^(s log2e - moff) for the masked score row (masked keys give 0), as
 // bf16 pairs into tensor memory; returns the fp32 sum of the probabilities.
-//
-// P in tensor memory is still read by the previous product: the first word is
-// computed before waiting for that product (`pv_bar`, `pv_parity`), the stores
-// come after. Returns false if the wait gave up.
 template <class C>
-__device__ __forceinline__ bool write_probabilities(const float* s, const uint32_t* m,
-                                                    const bool* live, int n_mma, float moff,
-                                                    uint32_t p_addr, const Sync& sy,
-                                                    uint32_t pv_bar, uint32_t pv_parity,
-                                                    float* sum) {
+__device__ __forceinline__ float write_probabilities(const float* s, const uint32_t* m,
+                                                     const bool* live, int n_mma, float moff,
+                                                     uint32_t p_addr) {
     const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
     const uint64_t neg2 = f2_pack(-moff, -moff);
     uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
@@ -445,18 +490,13 @@ __device__ __forceinline__ bool write_probabilities(const float* s, const uint32
 #pragma unroll
                 for (int j = 0; j < 16; ++j) pk[j] = 0u;
             }
-            if (q == 0) {
-                if (!sy.wait(pv_bar, pv_parity)) return false;
-                tc_fence_after();
-            }
             tmem_st16(p_addr + q * 16, pk);
         }
     }
     float a0, a1, b0, b1;
     f2_unpack(acc0, a0, a1);
     f2_unpack(acc1, b0, b1);
-    *sum = (a0 + a1) + (b0 + b1);
-    return true;
+    return (a0 + a1) + (b0 + b1);
 }
 
 // Maximum of the masked score row (-inf when the row has no key here).
@@ -486,13 +526,10 @@ __device__ __forceinline__ uint32_t swizzled_chunk(int row, int k, int rowb) {
 
 // Probabilities for the fast path: chunk row i holds keys [i*CWP, (i+1)*CWP)
 // and is either wholly in this row's H/T window (bit i of rowbits) or not;
-// keys outside the W window already carry -2^40 from the tensor core. The
-// first word is computed before waiting for the previous product.
+// keys outside the W window already carry -2^40 from the tensor core.
 template <class C>
-__device__ __forceinline__ bool fast_probabilities(const float* s, uint32_t rowbits, const bool* live,
-                                                   int n_mma, float moff, uint32_t p_addr,
-                                                   const Sync& sy, uint32_t pv_bar,
-                                                   uint32_t pv_parity, float* sum) {
+__device__ __forceinline__ float fast_probabilities(const float* s, uint32_t rowbits, const bool* live,
+                                                    int n_mma, float moff, uint32_t p_addr) {
     const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
     uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
@@ -522,18 +559,13 @@ __device__ __forceinline__ bool fast_probabilities(const float* s, uint32_t rowb
 #pragma unroll
                 for (int j = 0; j < 16; ++j) pk[j] = 0u;
             }
-            if (q == 0) {
-                if (!sy.wait(pv_bar, pv_parity)) return false;
-                tc_fence_after();
-            }
             tmem_st16(p_addr + q * 16, pk);
         }
     }
     float a0, a1, b0, b1;
     f2_unpack(acc0, a0, a1);
     f2_unpack(acc1, b0, b1);
-    *sum = (a0 + a1) + (b0 + b1);
-    return true;
+    return (a0 + a1) + (b0 + b1);
 }
 
 // Maximum over the valid chunk rows (W-masked keys sit at -2^40 and never win:
@@ -627,12 +659,21 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
         ChunkCursor cur{U.lo_t, 0, 0};
 
         for (int c = 0; c < U.nch; ++c, ++g) {
-            if (!sy.wait(sy.bar(C::B_SFULL), g & 1u)) return;
+            if (!sy.wait(sy.bar(C::B_SFULL + g % C::RING), (g / C::RING) & 1u)) return;
             tc_fence_after();
+            // this chunk's ring slot: S words 0.. start there (wrapping to the
+            // first slot after the last), and P goes over its first SW columns
+            const uint32_t slot = C::slot_of(g);
+            const uint32_t p_addr = t_row + C::TM_R + slot * C::SW;
             float s[C::NCAP];   // loaded asynchronously; not read before tmem_wait_ld
 #pragma unroll
-            for (int q = 0; q < C::NW; ++q)
-                if (q * 32 < p.n_mma) tmem_ld32(t_row + C::TM_S + q * 32, s + 32 * q);
+            for (int q = 0; q < C::NW; ++q) {
+                if (q * 32 < p.n_mma) {
+                    uint32_t sl = slot + (32u * q) / C::SW;
+                    sl = sl >= static_cast<uint32_t>(C::NSLOT) ? sl - C::NSLOT : sl;
+                    tmem_ld32(t_row + C::TM_R + sl * C::SW + (32u * q) % C::SW, s + 32 * q);
+                }
+            }
             // The window mask of this chunk is built while the score loads are in flight.
             // chunk geometry for this row (independent of the scores)
             const int kh0 = U.lo_h + cur.hc * p.cr, kw0 = U.lo_w + cur.wc * p.cw;
@@ -671,36 +712,20 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
 
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(sy.bar(C::B_SEMPTY));   // the next score tile may overwrite S now
+            mbar_arrive(sy.bar(C::B_SEMPTY + g % C::RING));   // these S columns may be overwritten now
 
-            // P and O are free once the previous product has completed
-            // (waited for inside the probability writer, after its first word).
-            const uint32_t pv_bar = sy.bar(C::B_PVDONE), pv_parity = (g & 1u) ^ 1u;
 
-            // Fast path: probabilities against the kept reference maximum,
-            // with no max pass. A row meeting its first keys, or a chunk whose
+            // Probabilities against the kept reference maximum, with no max
+            // pass. A row meeting its first keys, or a chunk whose
             // probabilities sum past 2^32 (its maximum grew by ~32 in log2
-            // units), takes the exact path: maximum, rescale, redo.
+            // units), takes an exact pass: maximum, reference update, redo.
             // Probabilities keep their relative precision at any scale, so
-            // both paths give the same result.
-            bool slow = __any_sync(0xffffffffu, has_keys && m_ref == -INFINITY);
-            float lsum = 0.f;
-            if (!slow) {
-                const float moff = m_ref == -INFINITY ? 0.f : m_ref;
-                bool ok;
-                if constexpr (C::FAST)
-                    ok = fast_probabilities<C>(s, rowbits, live, p.n_mma, moff, t_row + C::TM_P, sy,
-                                               pv_bar, pv_parity, &lsum);
-                else
-                    ok = write_probabilities<C>(s, m, live, p.n_mma, moff, t_row + C::TM_P, sy,
-                                                pv_bar, pv_parity, &lsum);
-                if (!ok) return;
-                slow = __any_sync(0xffffffffu, !(lsum <= kSumLimit));
-                if (slow) tmem_wait_st();   // the exact path overwrites this P
-            }
-            float alpha = 1.f;
+            // both passes give the same result.
+            bool exact = __any_sync(0xffffffffu, has_keys && m_ref == -INFINITY);
+            float lsum = 0.f, alpha = 1.f;
             bool rescale = false;
-            if (slow) {
+            // the reference update of an exact pass
+            auto exact_max = [&]() {
                 float mx;
                 if constexpr (C::FAST) mx = fast_row_max<C>(s, rowbits, live);
                 else mx = masked_row_max<C>(s, m, live);
@@ -712,19 +737,42 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
                     }
                     m_ref = mx2;
                 }
-                const float moff = m_ref == -INFINITY ? 0.f : m_ref;
-                bool ok;
-                if constexpr (C::FAST)
-                    ok = fast_probabilities<C>(s, rowbits, live, p.n_mma, moff, t_row + C::TM_P, sy,
-                                               pv_bar, pv_parity, &lsum);
-                else
-                    ok = write_probabilities<C>(s, m, live, p.n_mma, moff, t_row + C::TM_P, sy,
-                                                pv_bar, pv_parity, &lsum);
-                if (!ok) return;
+            };
+            if constexpr (C::FAST) {
+                // one copy of the probability code serves both passes (the
+                // loop is not unrolled), which keeps the loop body small
+#pragma unroll 1
+                for (;;) {
+                    if (exact) exact_max();
+                    lsum = fast_probabilities<C>(s, rowbits, live, p.n_mma,
+                                                 m_ref == -INFINITY ? 0.f : m_ref, p_addr);
+                    // after an exact pass every probability is at most 2^8
+                    if (exact || !__any_sync(0xffffffffu, !(lsum <= kSumLimit))) break;
+                    exact = true;
+                    tmem_wait_st();   // the exact pass overwrites this P
+                }
+            } else {
+                // per-key masks: the rolled form spills, so the passes are written out
+                if (!exact) {
+                    lsum = write_probabilities<C>(s, m, live, p.n_mma, m_ref == -INFINITY ? 0.f : m_ref,
+                                                  p_addr);
+                    exact = __any_sync(0xffffffffu, !(lsum <= kSumLimit));
+                    if (exact) tmem_wait_st();   // the exact pass overwrites this P
+                }
+                if (exact) {
+                    exact_max();
+                    lsum = write_probabilities<C>(s, m, live, p.n_mma, m_ref == -INFINITY ? 0.f : m_ref,
+                                                  p_addr);
+                }
             }
             l = l * alpha + lsum;
 
             if (__any_sync(0xffffffffu, rescale)) {
+                // O holds the products up to chunk g-1 (one of this unit: the
+                // reference maximum was finite); the last of them must be done
+                const uint32_t pc = g - 1u;
+                if (!sy.wait(sy.bar(C::B_PFREE + pc % C::RING), (pc / C::RING) & 1u)) return;
+                tc_fence_after();
                 const float a = rescale ? alpha : 1.f;
 #pragma unroll 1
                 for (int q = 0; q < C::OPIECES; ++q) {  // HD = 16 also scales 16 unused columns
@@ -738,7 +786,7 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(sy.bar(C::B_PFULL));
+            mbar_arrive(sy.bar(C::B_PFULL + g % C::RING));
         }
 
         // the next unit's W masks go out before this unit's epilogue
@@ -815,7 +863,9 @@ na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     Sync sy{base + C::OFF_BAR, misc + 1};
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NBAR; ++i) {
-            const bool softmax_arrives = i == C::B_SEMPTY || i == C::B_PFULL || i == C::B_OEMPTY ||
+            const bool softmax_arrives = i == C::B_OEMPTY ||
+                                         (i >= C::B_SEMPTY && i < C::B_SEMPTY + C::RING) ||
+                                         (i >= C::B_PFULL && i < C::B_PFULL + C::RING) ||
                                          (i >= C::B_XFULL && i < C::B_XFULL + C::NQX);
             mbar_init(sy.bar(i), softmax_arrives ? 128u : 1u);
         }
