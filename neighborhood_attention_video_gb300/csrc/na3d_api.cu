@@ -288,6 +288,8 @@ int na3d_fwd_strided(const void* q, const void* k, const void* v, void* out, int
     kp.div_nbw = na3d::make_fastdiv(kp.nbw);
     kp.div_nbh = na3d::make_fastdiv(kp.nbh);
     kp.div_nbt = na3d::make_fastdiv(kp.nbt);
+    kp.div_cr = na3d::make_fastdiv(kp.cr);
+    kp.div_cw = na3d::make_fastdiv(kp.cw);
 
     CUtensorMap tq, tk, tv;
     if (!encode_map(&tq, q, B, T, H, W, NH, HD, q_token_stride, vi.hd_box, pl.bw, pl.bh, pl.bt) ||

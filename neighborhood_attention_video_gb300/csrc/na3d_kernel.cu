@@ -183,8 +183,9 @@ __device__ __forceinline__ Unit unit_of(const KernelParams& p, int u) {
     const int hi_t = win_start(min(U.t0 + p.bt, p.T) - 1, p.KT, p.T) + p.KT;
     const int hi_h = win_start(min(U.h0 + p.bh, p.H) - 1, p.KH, p.H) + p.KH;
     const int hi_w = win_start(min(U.w0 + p.bw, p.W) - 1, p.KW, p.W) + p.KW;
-    U.n_hc = (hi_h - U.lo_h + p.cr - 1) / p.cr;
-    U.n_wc = (hi_w - U.lo_w + p.cw - 1) / p.cw;
+    int rem;
+    U.n_hc = fast_divmod(hi_h - U.lo_h + p.cr - 1, p.div_cr, &rem);
+    U.n_wc = fast_divmod(hi_w - U.lo_w + p.cw - 1, p.div_cw, &rem);
     U.nch = (hi_t - U.lo_t) * U.n_hc * U.n_wc;
     return U;
 }
@@ -214,6 +215,22 @@ __device__ __forceinline__ void bit_range128(uint32_t m[4], int a, int b) {
 
 // ------------------------------------------------------------------ waits
 
+// Spin on a barrier phase for at most kWaitLimitNs; on timeout, flag the CTA
+// (abort_flag, shared by all roles) and the device (g_na3d_timeout_flag).
+__device__ __forceinline__ bool wait_spin(uint32_t b, uint32_t parity, volatile uint32_t* abort_flag) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(b, parity)) return true;
+        if ((it & 1023u) == 0u) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1u;
+                atomicOr(&g_na3d_timeout_flag, 1u);
+                return false;
+            }
+        }
+    }
+}
 struct Sync {
     uint32_t bar0;                     // smem address of barrier 0
     volatile uint32_t* abort_flag;     // smem, shared by all roles
@@ -222,18 +239,7 @@ struct Sync {
     // Wait for a barrier phase; false once this CTA has given up.
     __device__ __forceinline__ bool wait(uint32_t b, uint32_t parity) const {
         if (mbar_try_wait(b, parity)) return true;
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t it = 1;; ++it) {
-            if (mbar_try_wait(b, parity)) return true;
-            if ((it & 1023u) == 0u) {
-                if (*abort_flag) return false;
-                if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                    *abort_flag = 1u;
-                    atomicOr(&g_na3d_timeout_flag, 1u);
-                    return false;
-                }
-            }
-        }
+        return wait_spin(b, parity, abort_flag);
     }
 };
 
@@ -281,6 +287,10 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tq, cons
                 tma_load_5d(base + C::OFF_K + st * C::KV_TILE + r * C::KV_REG, tk, full,
                             cc.x + r * C::HDB, cc.kw0, cc.kh0, cc.kt, cc.b);
             ++gk;
+            // V trails K by one chunk; it goes before the unit's Q brick, whose
+            // buffer may still be read by the previous unit's last score tile
+            if (gk >= 2 && !load_v(prev)) { ok = false; break; }
+            prev = cc;
             if (c == 0) {  // the Q brick goes right behind the unit's first K chunk
                 const uint32_t qb = ul % C::NQ;
                 if (!sy.wait(sy.bar(C::B_QEMPTY + qb), ((ul / C::NQ) & 1u) ^ 1u)) { ok = false; break; }
@@ -292,8 +302,6 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tq, cons
                                 xq + r * C::HDB, U.w0, U.h0, U.t0, U.b);
                 ++nq;
             }
-            if (gk >= 2 && !load_v(prev)) { ok = false; break; }   // V trails K by one chunk
-            prev = cc;
         }
     }
     if (ok && gk > gv) load_v(prev);
@@ -313,6 +321,7 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tq, cons
 // ------------------------------------------------------------------ tensor-core issuer
 
 // Walks the CTA's chunks in order: unit u (blockIdx.x, += gridDim.x), chunk c.
+// The unit's chunk count is decoded once, at its first chunk (one call site).
 struct ChunkWalk {
     int u, c, nch;
     uint32_t ul, g;   // local unit counter, global chunk counter
@@ -321,16 +330,20 @@ struct ChunkWalk {
         c = 0;
         ul = 0;
         g = 0;
-        nch = u < p.n_units ? unit_of(p, u).nch : 0;
+        nch = 0;
     }
-    __device__ __forceinline__ bool done(const KernelParams& p) const { return u >= p.n_units; }
-    __device__ __forceinline__ void next(const KernelParams& p) {
+    // false when the CTA has no units left; decodes a new unit's chunk count
+    __device__ __forceinline__ bool more(const KernelParams& p) {
+        if (u >= p.n_units) return false;
+        if (c == 0) nch = unit_of(p, u).nch;
+        return true;
+    }
+    __device__ __forceinline__ void next() {
         ++g;
         if (++c == nch) {
             c = 0;
             ++ul;
             u += gridDim.x;
-            nch = u < p.n_units ? unit_of(p, u).nch : 0;
         }
     }
 };
@@ -378,7 +391,7 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
     };
     ChunkWalk w;
     w.start(p);
-    while (!w.done(p)) {
+    while (w.more(p)) {
         const uint32_t qb = w.ul % C::NQ, st = w.g % C::NS;
         if (w.c == 0 && !sy.wait(sy.bar(C::B_QFULL + qb), (w.ul / C::NQ) & 1u)) break;
         uint32_t xb = 0;
@@ -417,7 +430,7 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
             umma_commit(sy.bar(C::B_QEMPTY + qb));
             if constexpr (C::FAST) umma_commit(sy.bar(C::B_XEMPTY + xb));
         }
-        w.next(p);
+        w.next();
     }
     // Drain: all MMAs issued by this thread complete before TMEM is freed.
     umma_commit(sy.bar(C::B_DRAIN));
@@ -435,7 +448,7 @@ __device__ void mma_pv_role(const KernelParams& p, const Sync& sy, uint32_t base
     const int ksteps = p.n_mma >> 4;
     ChunkWalk w;
     w.start(p);
-    while (!w.done(p)) {
+    while (w.more(p)) {
         const uint32_t st = w.g % C::NS;
         if (w.c == 0 && !sy.wait(sy.bar(C::B_OEMPTY), (w.ul & 1u) ^ 1u)) break;
         if (!sy.wait(sy.bar(C::B_VFULL + st), (w.g / C::NS) & 1u)) break;
@@ -452,7 +465,7 @@ __device__ void mma_pv_role(const KernelParams& p, const Sync& sy, uint32_t base
         umma_commit(sy.bar(C::B_PFREE + w.g % C::RING));
         umma_commit(sy.bar(C::B_VEMPTY + st));
         if (w.c == w.nch - 1) umma_commit(sy.bar(C::B_OFULL));
-        w.next(p);
+        w.next();
     }
     umma_commit(sy.bar(C::B_DRAIN2));
     mbar_wait_bounded(sy.bar(C::B_DRAIN2), 0, kDrainLimitNs);

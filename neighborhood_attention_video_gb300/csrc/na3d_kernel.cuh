@@ -36,6 +36,7 @@ struct KernelParams {
     int32_t n_units;         // B * nbt * nbh * nbw * NH
     uint16_t* out;           // bf16 output, (B,T,H,W,NH,HD)
     FastDiv div_nh, div_nbw, div_nbh, div_nbt;   // unit index decomposition
+    FastDiv div_cr, div_cw;                      // chunks per halo row group / W segment
 };
 
 // Compile-time shape of one kernel instance, as the planner needs it.
