@@ -614,13 +614,12 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
     const int iw = r % p.bw, ih = (r / p.bw) % p.bh, it = r / (p.bw * p.bh);
     uint32_t g = 0, ul = 0;
 
-    // Qx row of unit `u` (local index `v`): -2^40 where this row's query does
+    // Qx row of unit X (local index `v`): -2^40 where this row's query does
     // not see the chunk column, 0 elsewhere; published for the tensor core.
-    auto publish_qx = [&](uint32_t v, int u) -> bool {
+    auto publish_qx = [&](uint32_t v, const Unit& X) -> bool {
         if constexpr (C::FAST) {
             const uint32_t xb = v % C::NQX;
             if (!sy.wait(sy.bar(C::B_XEMPTY + xb), ((v / C::NQX) & 1u) ^ 1u)) return false;
-            const Unit X = unit_of(p, u);
             const int t = X.t0 + it, h = X.h0 + ih, w = X.w0 + iw;
             const bool ok = r < M && t < p.T && h < p.H && w < p.W;
             const int c_lo = win_start(w, p.KW, p.W) - X.lo_w;
@@ -645,19 +644,30 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
         return true;
     };
 
-    if (static_cast<int>(blockIdx.x) < p.n_units && !publish_qx(0, blockIdx.x)) return;
+    int u = blockIdx.x;
+    Unit U{};   // the unit being processed; decoded once, when its W masks go out
+    if (u < p.n_units) {
+        U = unit_of(p, u);
+        if (!publish_qx(0, U)) return;
+    }
+    // A finished unit's output is written once the next unit is set up, so its
+    // last product completes meanwhile; then the tensor memory O is released.
+    uint16_t* e_orow = nullptr;
+    float e_l = 0.f;
+    uint32_t e_ul = 0;
+    bool e_valid = false, e_live = false;
 
-    for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++ul) {
-        const Unit U = unit_of(p, u);
+    for (;; u += gridDim.x, ++ul) {
+        const bool have = u < p.n_units;
         const int t = U.t0 + it, h = U.h0 + ih, w = U.w0 + iw;
-        const bool valid = r < M && t < p.T && h < p.H && w < p.W;
+        const bool valid = have && r < M && t < p.T && h < p.H && w < p.W;
         const int sT = win_start(t, p.KT, p.T), sH = win_start(h, p.KH, p.H),
                   sW = win_start(w, p.KW, p.W);
         // Generic path: column pattern of this row's window inside one chunk
         // (when a chunk holds several h-rows, the W extent of the halo fits in cw).
         uint32_t rowpat[4] = {0u, 0u, 0u, 0u};
         if constexpr (!C::FAST) {
-            if (p.cr > 1) {
+            if (have && p.cr > 1) {
                 const int c0 = max(sW - U.lo_w, 0), c1 = min(sW + p.KW - U.lo_w, p.cw);
                 for (int i = 0; i < p.cr; ++i) {
                     uint32_t tmp[4];
@@ -667,6 +677,32 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
                 }
             }
         }
+        if (e_live) {   // the previous unit's epilogue: O / l -> bf16 -> global
+            if (!sy.wait(sy.bar(C::B_OFULL), e_ul & 1u)) return;
+            tc_fence_after();
+            const float inv = (e_valid && e_l > 0.f) ? rcp_approx(e_l) : 0.f;
+#pragma unroll 1
+            for (int q = 0; q < C::OPIECES; ++q) {
+                float o[32];
+                tmem_ld32(t_row + C::TM_O + q * 32, o);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(o[2 * j] * inv, o[2 * j + 1] * inv);
+                if (e_valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(e_orow + q * 32);
+                    constexpr int kVec = (C::HD < 32 ? C::HD : 32) / 8;   // 16-byte stores per piece
+#pragma unroll
+                    for (int i = 0; i < kVec; ++i)
+                        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(sy.bar(C::B_OEMPTY));
+            e_live = false;
+        }
+        if (!have) break;
+
         float m_ref = -INFINITY;   // reference maximum, log2 units
         float l = 0.f;             // running sum of the probabilities
         ChunkCursor cur{U.lo_t, 0, 0};
@@ -803,32 +839,16 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
         }
 
         // the next unit's W masks go out before this unit's epilogue
-        if (u + static_cast<int>(gridDim.x) < p.n_units && !publish_qx(ul + 1, u + gridDim.x)) return;
-
-        // epilogue: O / l -> bf16 -> global
-        if (!sy.wait(sy.bar(C::B_OFULL), ul & 1u)) return;
-        tc_fence_after();
-        const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
         const int64_t tok = ((static_cast<int64_t>(U.b) * p.T + t) * p.H + h) * p.W + w;
-        uint16_t* orow = p.out + (tok * p.NH + U.n) * C::HD;
-#pragma unroll 1
-        for (int q = 0; q < C::OPIECES; ++q) {
-            float o[32];
-            tmem_ld32(t_row + C::TM_O + q * 32, o);
-            tmem_wait_ld();
-            uint32_t pk[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(o[2 * j] * inv, o[2 * j + 1] * inv);
-            if (valid) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
-                constexpr int kVec = (C::HD < 32 ? C::HD : 32) / 8;   // 16-byte stores per piece
-#pragma unroll
-                for (int i = 0; i < kVec; ++i)
-                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            }
+        e_orow = p.out + (tok * p.NH + U.n) * C::HD;
+        e_l = l;
+        e_ul = ul;
+        e_valid = valid;
+        e_live = true;
+        if (u + static_cast<int>(gridDim.x) < p.n_units) {
+            U = unit_of(p, u + gridDim.x);
+            if (!publish_qx(ul + 1, U)) return;
         }
-        tc_fence_before();
-        mbar_arrive(sy.bar(C::B_OEMPTY));
     }
 }
 

@@ -278,6 +278,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // Two fp32 values rounded to bf16 (nearest even) and packed: lo in bits 0-15.
+// 1/x, approximate (relative error below 2^-22): enough for a bf16 result.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
