@@ -148,6 +148,21 @@ def test_axis_flip_equivariance():
         assert rel < 5e-3, (axis, rel)
 
 
+@pytest.mark.parametrize("kernel", [(3, 5, 7), (3, 7, 33)], ids=lambda x: "x".join(map(str, x)))
+def test_score_spike_in_a_later_chunk(kernel):
+    """Keys of the last frames are scaled up, so rows meet scores tens of log2
+    units above everything they saw in earlier chunks: the kept reference
+    maximum must be raised mid-row and O rescaled (the exact pass taken when a
+    chunk's probabilities sum past 2^32)."""
+    shape = (1, 6, 12, 36, 2, 64)
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=13)
+    kf = na3d_inputs.bf16_bits_to_f64(k)
+    kf[:, 4:] *= 40.0
+    k = na3d_inputs.f64_to_bf16_bits(kf)
+    got = run_gpu(q, k, v, kernel)
+    check(got, oracle.na3d_fwd(q, k, v, kernel), f"spike {shape} {kernel}")
+
+
 # ------------------------------------------------------------ launch behaviour
 
 def test_deterministic_and_stream_independent():
@@ -160,6 +175,31 @@ def test_deterministic_and_stream_independent():
         c = run_gpu(q, k, v, kernel, stream=s)
     np.testing.assert_array_equal(a, b)
     np.testing.assert_array_equal(a, c)
+
+
+@pytest.mark.parametrize("shape,kernel", [((1, 16, 64, 64, 8, 64), (3, 7, 7)),
+                                          ((1, 16, 64, 5, 8, 64), (3, 5, 5)),
+                                          ((2, 8, 48, 48, 8, 128), (3, 7, 7))],
+                         ids=lambda x: "x".join(map(str, x)))
+def test_repeated_launches_are_bit_identical(shape, kernel):
+    """Shapes with many work units per CTA: every per-chunk pipeline barrier
+    goes through many phases, and softmax warps can drift a chunk apart. A
+    barrier that lets one warp complete another chunk's phase shows up as
+    rows that differ between launches."""
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=11)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    first = None
+    for _ in range(6):
+        out = torch.full_like(qd, float("nan"))
+        na.na3d_fwd(qd, kd, vd, out, kernel)
+        torch.cuda.synchronize()
+        assert na.na3d_device_status() == 0
+        got = from_dev(out)
+        assert np.isfinite(na3d_inputs.bf16_bits_to_f64(got)).all()
+        if first is None:
+            first = got
+        else:
+            np.testing.assert_array_equal(got, first)
 
 
 def test_invalid_device_arguments_are_rejected():
