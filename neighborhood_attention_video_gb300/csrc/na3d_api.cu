@@ -284,6 +284,8 @@ int na3d_fwd_strided(const void* q, const void* k, const void* v, void* out, int
     if (units >= (int64_t(1) << 31)) return NA3D_ERR_OVERFLOW;
     kp.n_units = int32_t(units);
     kp.out = static_cast<uint16_t*>(out);
+    // rows are HD * 2 >= 32 bytes: 32-byte stores when the base allows them
+    kp.out_v8 = (reinterpret_cast<uintptr_t>(out) % 32u) == 0u ? 1 : 0;
     kp.div_nh = na3d::make_fastdiv(kp.NH);
     kp.div_nbw = na3d::make_fastdiv(kp.nbw);
     kp.div_nbh = na3d::make_fastdiv(kp.nbh);

@@ -690,11 +690,16 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
 #pragma unroll
                 for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(o[2 * j] * inv, o[2 * j + 1] * inv);
                 if (e_valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(e_orow + q * 32);
-                    constexpr int kVec = (C::HD < 32 ? C::HD : 32) / 8;   // 16-byte stores per piece
+                    constexpr int kBytes = (C::HD < 32 ? C::HD : 32) * 2;   // bytes per piece
+                    if (p.out_v8) {   // whole 32-byte sectors per lane
 #pragma unroll
-                    for (int i = 0; i < kVec; ++i)
-                        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        for (int i = 0; i < kBytes / 32; ++i) st_global_v8(e_orow + q * 32 + 16 * i, pk + 8 * i);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(e_orow + q * 32);
+#pragma unroll
+                        for (int i = 0; i < kBytes / 16; ++i)
+                            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
                 }
             }
             tc_fence_before();

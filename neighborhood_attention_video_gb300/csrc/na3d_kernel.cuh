@@ -35,6 +35,7 @@ struct KernelParams {
     int32_t cw, cr, n_mma;   // chunk geometry and score-tile width
     int32_t n_units;         // B * nbt * nbh * nbw * NH
     uint16_t* out;           // bf16 output, (B,T,H,W,NH,HD)
+    int32_t out_v8;          // 1: out is 32-byte aligned (32-byte stores), 0: 16-byte stores
     FastDiv div_nh, div_nbw, div_nbh, div_nbt;   // unit index decomposition
     FastDiv div_cr, div_cw;                      // chunks per halo row group / W segment
 };

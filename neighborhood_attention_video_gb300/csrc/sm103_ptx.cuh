@@ -278,6 +278,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // Two fp32 values rounded to bf16 (nearest even) and packed: lo in bits 0-15.
+// 32-byte global store (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* v) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 // 1/x, approximate (relative error below 2^-22): enough for a bf16 result.
 __device__ __forceinline__ float rcp_approx(float x) {
     float y;

@@ -226,13 +226,15 @@ def test_empty_batch_is_a_no_op():
     torch.cuda.synchronize()
 
 
-def test_output_untouched_outside_the_tensor():
+@pytest.mark.parametrize("shift", [0, 8], ids=["out32B", "out16B"])
+def test_output_untouched_outside_the_tensor(shift):
     """The kernel writes exactly the output tensor: guard bands around it keep
-    their sentinel values."""
+    their sentinel values. `shift` elements move the output off a 32-byte
+    boundary (16-byte stores instead of 32-byte ones)."""
     shape, kernel = (1, 5, 11, 13, 3, 64), (3, 5, 5)
     q, k, v = na3d_inputs.make_qkv(*shape, seed=5)
     n = int(np.prod(shape))
-    guard = 4096
+    guard = 4096 + shift
     buf = torch.full((n + 2 * guard,), 7.0, dtype=torch.bfloat16, device="cuda")
     out = buf[guard:guard + n].view(shape)
     na.na3d_fwd(to_dev(q), to_dev(k), to_dev(v), out, kernel)
