@@ -97,6 +97,38 @@ int na3d_fwd_strided(const void* q, const void* k, const void* v, void* out,
                      int64_t KT, int64_t KH, int64_t KW, int64_t q_token_stride,
                      int64_t k_token_stride, int64_t v_token_stride, void* stream);
 
+/*
+ * na3d_fwd_region - queries on a box of the grid, keys and values on the whole
+ * grid: out = NA3D(q, k, v) restricted to the grid positions (t0 + t, h0 + h,
+ * w0 + w), 0 <= t < Tq, 0 <= h < Hq, 0 <= w < Wq. Every query keeps the window
+ * it has in the whole grid (global coordinates, shifted inward at the grid's
+ * borders, never at the box's), so the result equals the matching rows of
+ * na3d_fwd on the whole grid. This generalises the test reference's
+ * `w_offset` mode ("[Triton/Gluon] Add 3D neighborhood flash attention
+ * (na3d_flash)", Technical Details, test file: q a W sub-slice, k and v the
+ * full tensors, bounds in global W coordinates) to a box on all three axes:
+ * tiles of a decoded video are computed with exact borders.
+ *
+ * q: (B, Tq, Hq, Wq, NH, HD) tokens with q_token_stride elements between
+ *   consecutive positions of the box (heads packed).
+ * k, v: (B, T, H, W, NH, HD), the whole grid, with k_token_stride and
+ *   v_token_stride elements between consecutive grid positions.
+ * out: contiguous (B, Tq, Hq, Wq, NH, HD); must not overlap the memory that
+ *   q, k or v span.
+ * t0, h0, w0 >= 0 and Tq, Hq, Wq >= 1 with t0 + Tq <= T, h0 + Hq <= H,
+ *   w0 + Wq <= W; otherwise NA3D_ERR_SHAPE. Windows satisfy KT <= T,
+ *   KH <= H, KW <= W (the box may be narrower than a window).
+ * All other arguments, the errors and the asynchrony are those of
+ * na3d_fwd_strided; na3d_fwd_strided is this call with the whole grid as the
+ * box (t0 = h0 = w0 = 0, Tq = T, Hq = H, Wq = W).
+ */
+int na3d_fwd_region(const void* q, const void* k, const void* v, void* out,
+                    int64_t B, int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD,
+                    int64_t KT, int64_t KH, int64_t KW,
+                    int64_t t0, int64_t h0, int64_t w0, int64_t Tq, int64_t Hq, int64_t Wq,
+                    int64_t q_token_stride, int64_t k_token_stride, int64_t v_token_stride,
+                    void* stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* na3d_status_string(int status);
 

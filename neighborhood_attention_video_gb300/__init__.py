@@ -13,14 +13,15 @@ import ctypes
 import os
 
 __all__ = [
-    "NA3DError", "NA3DUnavailable", "na3d_fwd", "na3d_fwd_strided", "na3d_status_string", "na3d_plan",
+    "NA3DError", "NA3DUnavailable", "na3d_fwd", "na3d_fwd_strided", "na3d_fwd_region",
+    "na3d_status_string", "na3d_plan",
     "na3d_device_status", "library_path", "load_library", "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libna3d.so")
-EXPORTED_SYMBOLS = ("na3d_fwd", "na3d_fwd_strided", "na3d_status_string", "na3d_plan",
-                    "na3d_device_status")
+EXPORTED_SYMBOLS = ("na3d_fwd", "na3d_fwd_strided", "na3d_fwd_region", "na3d_status_string",
+                    "na3d_plan", "na3d_device_status")
 
 NA3D_OK = 0
 _I64 = ctypes.c_int64
@@ -66,6 +67,8 @@ def load_library():
     lib.na3d_fwd.restype = ctypes.c_int
     lib.na3d_fwd_strided.argtypes = [_P, _P, _P, _P] + [_I64] * 12 + [_P]
     lib.na3d_fwd_strided.restype = ctypes.c_int
+    lib.na3d_fwd_region.argtypes = [_P, _P, _P, _P] + [_I64] * 18 + [_P]
+    lib.na3d_fwd_region.restype = ctypes.c_int
     lib.na3d_status_string.argtypes = [ctypes.c_int]
     lib.na3d_status_string.restype = ctypes.c_char_p
     lib.na3d_plan.argtypes = [_I64] * 8 + [ctypes.POINTER(PlanInfo)]
@@ -149,6 +152,39 @@ def na3d_fwd_strided(q, k, v, out, kernel_size, stream=None) -> None:
                               _stream_handle(stream))
     if rc != NA3D_OK:
         raise NA3DError(rc, "na3d_fwd_strided")
+
+
+def na3d_fwd_region(q, k, v, out, kernel_size, offset, stream=None) -> None:
+    """``out`` = the rows of NA3D on the whole grid at the query box
+    ``offset`` = (t0, h0, w0) with the extents of ``q``: q and out have shape
+    (B, Tq, Hq, Wq, NH, HD), k and v (B, T, H, W, NH, HD). Every query keeps
+    its window in the whole grid (global coordinates). q, k, v may be views
+    with a token stride as in ``na3d_fwd_strided``; ``out`` is contiguous."""
+    import torch
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a bfloat16 CUDA tensor")
+        if t.dim() != 6:
+            raise ValueError(f"{name} must be a 6-D tensor")
+    if tuple(k.shape) != tuple(v.shape) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("k and v must share a shape, and so must q and out")
+    if q.shape[0] != k.shape[0] or q.shape[4:] != k.shape[4:]:
+        raise ValueError("q and k must agree on B, NH and HD")
+    if not out.is_contiguous():
+        raise ValueError("out must be contiguous")
+    strides = [_token_stride(n, t) for n, t in (("q", q), ("k", k), ("v", v))]
+    KT, KH, KW = (int(x) for x in kernel_size)
+    t0, h0, w0 = (int(x) for x in offset)
+    B, T, H, W, NH, HD = (int(x) for x in k.shape)
+    Tq, Hq, Wq = (int(x) for x in q.shape[1:4])
+    rc = lib.na3d_fwd_region(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             B, T, H, W, NH, HD, KT, KH, KW, t0, h0, w0, Tq, Hq, Wq,
+                             *strides, _stream_handle(stream))
+    if rc != NA3D_OK:
+        raise NA3DError(rc, "na3d_fwd_region")
 
 
 def na3d_plan(T, H, W, NH, HD, KT, KH, KW) -> dict:

@@ -54,14 +54,20 @@ int64_t win_start(int64_t i, int64_t K, int64_t N) {
     return s;
 }
 
+// One axis of the problem: `nq` query positions starting at `off` of an axis
+// of length `n` (the whole axis: off = 0, nq = n), windows of length `k`.
+struct Axis {
+    int64_t nq, off, n, k;
+};
+
 // Sum over the bricks of one axis of ceil(extent / unit), where extent is the
 // length of the union of the windows of the brick's queries (unit 1: the
 // union length itself). Also returns the number of bricks.
-int64_t axis_sum(int64_t N, int64_t K, int64_t b, int64_t unit, int64_t* nbricks) {
+int64_t axis_sum(const Axis& a, int64_t b, int64_t unit, int64_t* nbricks) {
     int64_t sum = 0, cnt = 0;
-    for (int64_t p0 = 0; p0 < N; p0 += b, ++cnt) {
-        const int64_t last = (p0 + b < N ? p0 + b : N) - 1;
-        const int64_t ext = win_start(last, K, N) + K - win_start(p0, K, N);
+    for (int64_t p0 = 0; p0 < a.nq; p0 += b, ++cnt) {
+        const int64_t last = a.off + (p0 + b < a.nq ? p0 + b : a.nq) - 1;
+        const int64_t ext = win_start(last, a.k, a.n) + a.k - win_start(a.off + p0, a.k, a.n);
         sum += (ext + unit - 1) / unit;
     }
     *nbricks = cnt;
@@ -84,9 +90,10 @@ constexpr double kChunkOverhead = 24.0;
 constexpr double kBrickOverhead = 96.0;
 constexpr double kFastColumn = 0.55;
 
-Plan make_plan(int64_t T, int64_t H, int64_t W, int64_t KT, int64_t KH, int64_t KW, int ncap) {
+Plan make_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap) {
+    const int64_t H = ah.n, W = aw.n, KH = ah.k, KW = aw.k;
     Plan best;
-    for (int64_t bw = 1; bw <= (W < 128 ? W : 128); ++bw) {
+    for (int64_t bw = 1; bw <= (aw.nq < 128 ? aw.nq : 128); ++bw) {
         const int64_t ew = (bw + KW - 1 < W) ? bw + KW - 1 : W;   // widest W union
         // W unions of up to 32 keys use a fixed power-of-two chunk stride and
         // the tensor-core W mask; wider ones the generic per-key masks.
@@ -95,17 +102,17 @@ Plan make_plan(int64_t T, int64_t H, int64_t W, int64_t KT, int64_t KH, int64_t 
         const int64_t cw = cwp ? cwp : (ew > ncap ? ncap : ew);
         const double col_cost = cwp ? kFastColumn : 1.0;
         int64_t nbw;
-        const int64_t sw = axis_sum(W, KW, bw, cw, &nbw);
-        for (int64_t bh = 1; bh <= H && bw * bh <= 128; ++bh) {
+        const int64_t sw = axis_sum(aw, bw, cw, &nbw);
+        for (int64_t bh = 1; bh <= ah.nq && bw * bh <= 128; ++bh) {
             const int64_t eh = (bh + KH - 1 < H) ? bh + KH - 1 : H;
             int64_t cr = (!cwp && ew > ncap) ? 1 : ncap / cw;
             if (cr > eh) cr = eh;
             const int64_t n_mma = (cr * cw + 15) / 16 * 16;
             int64_t nbh;
-            const int64_t sh = axis_sum(H, KH, bh, cr, &nbh);
-            for (int64_t bt = 1; bt <= T && bw * bh * bt <= 128; ++bt) {
+            const int64_t sh = axis_sum(ah, bh, cr, &nbh);
+            for (int64_t bt = 1; bt <= at.nq && bw * bh * bt <= 128; ++bt) {
                 int64_t nbt;
-                const int64_t st = axis_sum(T, KT, bt, 1, &nbt);
+                const int64_t st = axis_sum(at, bt, 1, &nbt);
                 const int64_t chunks = st * sh * sw;
                 const int64_t bricks = nbt * nbh * nbw;
                 const double cost = double(chunks) * (double(n_mma) * col_cost + kChunkOverhead) +
@@ -125,19 +132,22 @@ Plan make_plan(int64_t T, int64_t H, int64_t W, int64_t KT, int64_t KH, int64_t 
     return best;
 }
 
-// Plans depend only on the grid, the window and the score-tile cap; they are
-// cached (bounded, mutex-guarded) because the search takes ~0.1 ms.
-Plan cached_plan(int64_t T, int64_t H, int64_t W, int64_t KT, int64_t KH, int64_t KW, int ncap) {
-    using Key = std::tuple<int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int>;
+// Plans depend only on the grid, the query box, the window and the
+// score-tile cap; they are cached (bounded, mutex-guarded) because the search
+// takes ~0.1 ms.
+Plan cached_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap) {
+    using Key = std::tuple<int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t,
+                           int64_t, int64_t, int64_t, int64_t, int>;
     static std::mutex mu;
     static std::map<Key, Plan> cache;
-    const Key key{T, H, W, KT, KH, KW, ncap};
+    const Key key{at.nq, at.off, at.n, at.k, ah.nq, ah.off, ah.n, ah.k,
+                  aw.nq, aw.off, aw.n, aw.k, ncap};
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
-    Plan pl = make_plan(T, H, W, KT, KH, KW, ncap);
+    Plan pl = make_plan(at, ah, aw, ncap);
     std::lock_guard<std::mutex> g(mu);
     if (cache.size() >= 1024) cache.clear();
     cache.emplace(key, pl);
@@ -220,7 +230,7 @@ int na3d_plan(int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t K
     if (rc != NA3D_OK) return rc;
     VariantInfo vi;
     if (!na3d::variant_info(int(HD), 0, &vi)) return NA3D_ERR_UNSUPPORTED;
-    const Plan pl = cached_plan(T, H, W, KT, KH, KW, vi.ncap);
+    const Plan pl = cached_plan(Axis{T, 0, T, KT}, Axis{H, 0, H, KH}, Axis{W, 0, W, KW}, vi.ncap);
     if (!na3d::variant_info(int(HD), pl.cwp, &vi)) return NA3D_ERR_UNSUPPORTED;
     info->bt = pl.bt; info->bh = pl.bh; info->bw = pl.bw;
     info->cw = pl.cw; info->cr = pl.cr; info->n_mma = pl.n_mma;
@@ -232,31 +242,38 @@ int na3d_plan(int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t K
     return NA3D_OK;
 }
 
-int na3d_fwd_strided(const void* q, const void* k, const void* v, void* out, int64_t B, int64_t T,
-                     int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT, int64_t KH,
-                     int64_t KW, int64_t q_token_stride, int64_t k_token_stride,
-                     int64_t v_token_stride, void* stream) {
+int na3d_fwd_region(const void* q, const void* k, const void* v, void* out, int64_t B, int64_t T,
+                    int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT, int64_t KH, int64_t KW,
+                    int64_t t0, int64_t h0, int64_t w0, int64_t Tq, int64_t Hq, int64_t Wq,
+                    int64_t q_token_stride, int64_t k_token_stride, int64_t v_token_stride,
+                    void* stream) {
     int rc = validate_shape(B, T, H, W, NH, HD, KT, KH, KW);
     if (rc != NA3D_OK) return rc;
-    const int64_t bytes = B * T * H * W * NH * HD * 2;
-    if (bytes == 0) return NA3D_OK;  // B == 0 or NH == 0: nothing to read or write
+    // the query box lies inside the grid
+    if (Tq < 1 || Hq < 1 || Wq < 1 || t0 < 0 || h0 < 0 || w0 < 0 || t0 > T - Tq || h0 > H - Hq ||
+        w0 > W - Wq)
+        return NA3D_ERR_SHAPE;
+    const int64_t kv_tokens = B * T * H * W, q_tokens = B * Tq * Hq * Wq;
+    const int64_t out_bytes = q_tokens * NH * HD * 2;
+    if (out_bytes == 0) return NA3D_OK;  // B == 0 or NH == 0: nothing to read or write
     if (!q || !k || !v || !out) return NA3D_ERR_NULL;
     const int64_t strides[3] = {q_token_stride, k_token_stride, v_token_stride};
+    const int64_t tokens[3] = {q_tokens, kv_tokens, kv_tokens};
+    const int64_t grid_tokens[3] = {Tq * Hq * Wq, T * H * W, T * H * W};
     int64_t spans[3];
-    const int64_t tokens = B * T * H * W;
     for (int i = 0; i < 3; ++i) {
         if (strides[i] < NH * HD) return NA3D_ERR_SHAPE;
         if ((strides[i] * 2) % 16 != 0) return NA3D_ERR_ALIGN;
         int64_t span;
-        if (!mul_ok(tokens - 1, strides[i], &span) || !mul_ok(span + NH * HD, 2, &spans[i]) ||
-            strides[i] * 2 >= (int64_t(1) << 40) / (W * H * T > 0 ? W * H * T : 1))
+        if (!mul_ok(tokens[i] - 1, strides[i], &span) || !mul_ok(span + NH * HD, 2, &spans[i]) ||
+            strides[i] * 2 >= (int64_t(1) << 40) / grid_tokens[i])
             return NA3D_ERR_OVERFLOW;
     }
     const void* ptrs[4] = {q, k, v, out};
     for (const void* p : ptrs)
         if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return NA3D_ERR_ALIGN;
-    if (overlaps(out, bytes, q, spans[0]) || overlaps(out, bytes, k, spans[1]) ||
-        overlaps(out, bytes, v, spans[2]))
+    if (overlaps(out, out_bytes, q, spans[0]) || overlaps(out, out_bytes, k, spans[1]) ||
+        overlaps(out, out_bytes, v, spans[2]))
         return NA3D_ERR_ALIAS;
 
     int dev = 0, major = 0, minor = 0, sms = 0;
@@ -269,16 +286,18 @@ int na3d_fwd_strided(const void* q, const void* k, const void* v, void* out, int
 
     VariantInfo vi;
     if (!na3d::variant_info(int(HD), 0, &vi)) return NA3D_ERR_UNSUPPORTED;
-    const Plan pl = cached_plan(T, H, W, KT, KH, KW, vi.ncap);
+    const Plan pl = cached_plan(Axis{Tq, t0, T, KT}, Axis{Hq, h0, H, KH}, Axis{Wq, w0, W, KW}, vi.ncap);
     if (!na3d::variant_info(int(HD), pl.cwp, &vi)) return NA3D_ERR_UNSUPPORTED;
 
     KernelParams kp;
     kp.B = int32_t(B); kp.T = int32_t(T); kp.H = int32_t(H); kp.W = int32_t(W); kp.NH = int32_t(NH);
+    kp.Tq = int32_t(Tq); kp.Hq = int32_t(Hq); kp.Wq = int32_t(Wq);
+    kp.t_off = int32_t(t0); kp.h_off = int32_t(h0); kp.w_off = int32_t(w0);
     kp.KT = int32_t(KT); kp.KH = int32_t(KH); kp.KW = int32_t(KW);
     kp.bt = pl.bt; kp.bh = pl.bh; kp.bw = pl.bw;
-    kp.nbt = int32_t((T + pl.bt - 1) / pl.bt);
-    kp.nbh = int32_t((H + pl.bh - 1) / pl.bh);
-    kp.nbw = int32_t((W + pl.bw - 1) / pl.bw);
+    kp.nbt = int32_t((Tq + pl.bt - 1) / pl.bt);
+    kp.nbh = int32_t((Hq + pl.bh - 1) / pl.bh);
+    kp.nbw = int32_t((Wq + pl.bw - 1) / pl.bw);
     kp.cw = pl.cw; kp.cr = pl.cr; kp.n_mma = pl.n_mma;
     const int64_t units = B * int64_t(kp.nbt) * kp.nbh * kp.nbw * NH;
     if (units >= (int64_t(1) << 31)) return NA3D_ERR_OVERFLOW;
@@ -293,8 +312,9 @@ int na3d_fwd_strided(const void* q, const void* k, const void* v, void* out, int
     kp.div_cr = na3d::make_fastdiv(kp.cr);
     kp.div_cw = na3d::make_fastdiv(kp.cw);
 
+    // Q over the query box, K and V over the whole grid
     CUtensorMap tq, tk, tv;
-    if (!encode_map(&tq, q, B, T, H, W, NH, HD, q_token_stride, vi.hd_box, pl.bw, pl.bh, pl.bt) ||
+    if (!encode_map(&tq, q, B, Tq, Hq, Wq, NH, HD, q_token_stride, vi.hd_box, pl.bw, pl.bh, pl.bt) ||
         !encode_map(&tk, k, B, T, H, W, NH, HD, k_token_stride, vi.hd_box, pl.cw, pl.cr, 1) ||
         !encode_map(&tv, v, B, T, H, W, NH, HD, v_token_stride, vi.hd_box, pl.cw, pl.cr, 1))
         return NA3D_ERR_CUDA;
@@ -305,6 +325,14 @@ int na3d_fwd_strided(const void* q, const void* k, const void* v, void* out, int
         cudaSuccess)
         return NA3D_ERR_CUDA;
     return NA3D_OK;
+}
+
+int na3d_fwd_strided(const void* q, const void* k, const void* v, void* out, int64_t B, int64_t T,
+                     int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT, int64_t KH,
+                     int64_t KW, int64_t q_token_stride, int64_t k_token_stride,
+                     int64_t v_token_stride, void* stream) {
+    return na3d_fwd_region(q, k, v, out, B, T, H, W, NH, HD, KT, KH, KW, 0, 0, 0, T, H, W,
+                           q_token_stride, k_token_stride, v_token_stride, stream);
 }
 
 int na3d_fwd(const void* q, const void* k, const void* v, void* out, int64_t B, int64_t T,

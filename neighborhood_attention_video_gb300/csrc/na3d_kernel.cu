@@ -174,15 +174,16 @@ __device__ __forceinline__ Unit unit_of(const KernelParams& p, int u) {
     u = fast_divmod(u, p.div_nbw, &iw);
     u = fast_divmod(u, p.div_nbh, &ih);
     U.b = fast_divmod(u, p.div_nbt, &it);
-    U.t0 = it * p.bt;
+    U.t0 = it * p.bt;   // brick origin in the query box
     U.h0 = ih * p.bh;
     U.w0 = iw * p.bw;
-    U.lo_t = win_start(U.t0, p.KT, p.T);
-    U.lo_h = win_start(U.h0, p.KH, p.H);
-    U.lo_w = win_start(U.w0, p.KW, p.W);
-    const int hi_t = win_start(min(U.t0 + p.bt, p.T) - 1, p.KT, p.T) + p.KT;
-    const int hi_h = win_start(min(U.h0 + p.bh, p.H) - 1, p.KH, p.H) + p.KH;
-    const int hi_w = win_start(min(U.w0 + p.bw, p.W) - 1, p.KW, p.W) + p.KW;
+    // halo in grid coordinates: windows of the brick's first and last queries
+    U.lo_t = win_start(p.t_off + U.t0, p.KT, p.T);
+    U.lo_h = win_start(p.h_off + U.h0, p.KH, p.H);
+    U.lo_w = win_start(p.w_off + U.w0, p.KW, p.W);
+    const int hi_t = win_start(p.t_off + min(U.t0 + p.bt, p.Tq) - 1, p.KT, p.T) + p.KT;
+    const int hi_h = win_start(p.h_off + min(U.h0 + p.bh, p.Hq) - 1, p.KH, p.H) + p.KH;
+    const int hi_w = win_start(p.w_off + min(U.w0 + p.bw, p.Wq) - 1, p.KW, p.W) + p.KW;
     int rem;
     U.n_hc = fast_divmod(hi_h - U.lo_h + p.cr - 1, p.div_cr, &rem);
     U.n_wc = fast_divmod(hi_w - U.lo_w + p.cw - 1, p.div_cw, &rem);
@@ -621,8 +622,8 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
             const uint32_t xb = v % C::NQX;
             if (!sy.wait(sy.bar(C::B_XEMPTY + xb), ((v / C::NQX) & 1u) ^ 1u)) return false;
             const int t = X.t0 + it, h = X.h0 + ih, w = X.w0 + iw;
-            const bool ok = r < M && t < p.T && h < p.H && w < p.W;
-            const int c_lo = win_start(w, p.KW, p.W) - X.lo_w;
+            const bool ok = r < M && t < p.Tq && h < p.Hq && w < p.Wq;
+            const int c_lo = win_start(p.w_off + w, p.KW, p.W) - X.lo_w;
             const uint32_t tile = base + C::OFF_QX + xb * C::QX_TILE;
 #pragma unroll
             for (int k = 0; k < C::XROWB / 16; ++k) {
@@ -660,9 +661,10 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
     for (;; u += gridDim.x, ++ul) {
         const bool have = u < p.n_units;
         const int t = U.t0 + it, h = U.h0 + ih, w = U.w0 + iw;
-        const bool valid = have && r < M && t < p.T && h < p.H && w < p.W;
-        const int sT = win_start(t, p.KT, p.T), sH = win_start(h, p.KH, p.H),
-                  sW = win_start(w, p.KW, p.W);
+        const bool valid = have && r < M && t < p.Tq && h < p.Hq && w < p.Wq;
+        // this row's window, in grid coordinates
+        const int sT = win_start(p.t_off + t, p.KT, p.T), sH = win_start(p.h_off + h, p.KH, p.H),
+                  sW = win_start(p.w_off + w, p.KW, p.W);
         // Generic path: column pattern of this row's window inside one chunk
         // (when a chunk holds several h-rows, the W extent of the halo fits in cw).
         uint32_t rowpat[4] = {0u, 0u, 0u, 0u};
@@ -844,7 +846,7 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
         }
 
         // the next unit's W masks go out before this unit's epilogue
-        const int64_t tok = ((static_cast<int64_t>(U.b) * p.T + t) * p.H + h) * p.W + w;
+        const int64_t tok = ((static_cast<int64_t>(U.b) * p.Tq + t) * p.Hq + h) * p.Wq + w;
         e_orow = p.out + (tok * p.NH + U.n) * C::HD;
         e_l = l;
         e_ul = ul;

@@ -28,13 +28,15 @@ inline FastDiv make_fastdiv(int32_t d) {
 
 // Everything the kernel needs besides the three TMA descriptors.
 struct KernelParams {
-    int32_t B, T, H, W, NH;
+    int32_t B, T, H, W, NH;          // key/value grid
+    int32_t Tq, Hq, Wq;              // query box extents (the whole grid unless a region is given)
+    int32_t t_off, h_off, w_off;     // query box origin in the grid
     int32_t KT, KH, KW;
     int32_t bt, bh, bw;      // query brick
-    int32_t nbt, nbh, nbw;   // bricks per axis
+    int32_t nbt, nbh, nbw;   // bricks per axis of the query box
     int32_t cw, cr, n_mma;   // chunk geometry and score-tile width
     int32_t n_units;         // B * nbt * nbh * nbw * NH
-    uint16_t* out;           // bf16 output, (B,T,H,W,NH,HD)
+    uint16_t* out;           // bf16 output, (B,Tq,Hq,Wq,NH,HD)
     int32_t out_v8;          // 1: out is 32-byte aligned (32-byte stores), 0: 16-byte stores
     FastDiv div_nh, div_nbw, div_nbh, div_nbt;   // unit index decomposition
     FastDiv div_cr, div_cw;                      // chunks per halo row group / W segment

@@ -243,6 +243,85 @@ def test_output_untouched_outside_the_tensor(shift):
     check(from_dev(out.contiguous()), oracle.na3d_fwd(q, k, v, kernel), "guarded")
 
 
+# ------------------------------------------------------------ query boxes (global coordinates)
+
+REGION_CASES = [
+    # (B, T, H, W, NH, HD), kernel, (t0, h0, w0, Tq, Hq, Wq)
+    ((1, 6, 12, 40, 2, 64), (3, 5, 7), (0, 0, 24, 6, 12, 16)),     # right W tile, as in tiled decode
+    ((1, 8, 16, 20, 2, 64), (3, 5, 5), (2, 3, 5, 4, 8, 9)),        # interior box on every axis
+    ((1, 5, 9, 30, 2, 32), (3, 5, 11), (1, 2, 10, 2, 4, 4)),       # box narrower than the window
+    ((1, 6, 10, 24, 2, 64), (5, 5, 5), (3, 5, 20, 3, 5, 4)),       # box at the far borders
+    ((2, 5, 13, 19, 3, 128), (3, 5, 7), (1, 2, 3, 3, 8, 10)),      # HD 128, B and NH > 1
+    ((1, 4, 9, 50, 2, 64), (3, 3, 33), (0, 0, 7, 4, 9, 30)),       # wide window: per-key masks
+]
+
+
+def region_oracle(q_full, k, v, kernel, box):
+    """The oracle on the whole grid, restricted to the box: a query's output
+    depends only on its own q and on k, v (global windows)."""
+    t0, h0, w0, Tq, Hq, Wq = box
+    full = oracle.na3d_fwd(q_full, k, v, kernel)
+    return full[:, t0:t0 + Tq, h0:h0 + Hq, w0:w0 + Wq]
+
+
+@pytest.mark.parametrize("shape,kernel,box", REGION_CASES, ids=lambda x: "x".join(map(str, x)))
+def test_region_matches_the_whole_grid_oracle(shape, kernel, box):
+    q_full, k, v = na3d_inputs.make_qkv(*shape, seed=17)
+    t0, h0, w0, Tq, Hq, Wq = box
+    q = np.ascontiguousarray(q_full[:, t0:t0 + Tq, h0:h0 + Hq, w0:w0 + Wq])
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    out = torch.empty_like(qd)
+    na.na3d_fwd_region(qd, kd, vd, out, kernel, (t0, h0, w0))
+    torch.cuda.synchronize()
+    assert na.na3d_device_status() == 0
+    check(from_dev(out), region_oracle(q_full, k, v, kernel, box), f"region {shape} {kernel} {box}")
+
+
+def test_region_of_the_whole_grid_is_na3d_fwd():
+    shape, kernel = (1, 6, 20, 36, 2, 64), (3, 7, 7)
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=19)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    out = torch.empty_like(qd)
+    na.na3d_fwd_region(qd, kd, vd, out, kernel, (0, 0, 0))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(from_dev(out), run_gpu(q, k, v, kernel))
+
+
+def test_w_tiles_reassemble_the_whole_output():
+    """Tiled decode: the W axis cut into tiles, each tile's queries attending
+    to the whole grid, reassembles the untiled result (within the bar)."""
+    shape, kernel = (1, 6, 16, 48, 2, 64), (3, 7, 9)
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=23)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    tiles = []
+    for w0, w1 in ((0, 20), (20, 29), (29, 48)):
+        out = torch.empty((1, 6, 16, w1 - w0, 2, 64), dtype=torch.bfloat16, device="cuda")
+        na.na3d_fwd_region(qd[:, :, :, w0:w1].contiguous(), kd, vd, out, kernel, (0, 0, w0))
+        tiles.append(out)
+    torch.cuda.synchronize()
+    got = from_dev(torch.cat(tiles, dim=3).contiguous())
+    check(got, oracle.na3d_fwd(q, k, v, kernel), "W tiles")
+
+
+def test_region_with_strided_views():
+    """The box's q and the whole grid's k, v as slices of fused projection outputs."""
+    shape, kernel, box = (1, 6, 12, 28, 2, 64), (3, 5, 7), (1, 2, 9, 4, 8, 12)
+    t0, h0, w0, Tq, Hq, Wq = box
+    q_full, k, v = na3d_inputs.make_qkv(*shape, seed=29)
+    fused = np.stack([q_full, k, v], axis=4)          # (B, T, H, W, 3, NH, HD)
+    fd = torch.from_numpy(fused.view(np.int16)).cuda().view(torch.bfloat16)
+    qv = fd[:, t0:t0 + Tq, h0:h0 + Hq, w0:w0 + Wq, 0]
+    assert not qv.is_contiguous()
+    out = torch.empty((1, Tq, Hq, Wq, 2, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):          # a box view of the grid has no single token stride
+        na.na3d_fwd_region(qv, fd[:, :, :, :, 1], fd[:, :, :, :, 2], out, kernel, (t0, h0, w0))
+    qb = torch.from_numpy(np.stack([q_full[:, t0:t0 + Tq, h0:h0 + Hq, w0:w0 + Wq]] * 3, axis=4)
+                          .view(np.int16)).cuda().view(torch.bfloat16)[:, :, :, :, 1]
+    na.na3d_fwd_region(qb, fd[:, :, :, :, 1], fd[:, :, :, :, 2], out, kernel, (t0, h0, w0))
+    torch.cuda.synchronize()
+    check(from_dev(out), region_oracle(q_full, k, v, kernel, box), "strided region")
+
+
 # ------------------------------------------------------------ strided (fused QKV) inputs
 
 @pytest.mark.parametrize("shape,kernel", [((1, 6, 20, 36, 2, 64), (3, 7, 7)),

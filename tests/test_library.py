@@ -104,6 +104,36 @@ def test_strided_validation(lib):
                         (3 * nhd,) * 3) == ERR_ALIAS
 
 
+def call_region(lib, ptrs, box, dims=(1, 4, 8, 16, 2, 32), kernel=(3, 5, 5), strides=None):
+    nhd = dims[4] * dims[5]
+    strides = strides or (nhd, nhd, nhd)
+    return lib.na3d_fwd_region(*[ctypes.c_void_p(p) for p in ptrs], *dims, *kernel, *box,
+                               *strides, None)
+
+
+def test_region_validation(lib):
+    """The query box (t0, h0, w0, Tq, Hq, Wq) must lie inside the grid."""
+    import torch
+    expect = OK if torch.cuda.is_available() else ERR_CUDA
+    base = 1 << 20
+    ptrs = (base, base + (1 << 22), base + (2 << 22), base + (3 << 22))
+    T, H, W = 4, 8, 16
+    assert call_region(lib, ptrs, (0, 0, 0, T, H, W)) == expect          # the whole grid
+    assert call_region(lib, ptrs, (1, 2, 9, 2, 5, 7)) == expect          # an interior box
+    assert call_region(lib, ptrs, (0, 0, 12, T, H, 2)) == expect         # narrower than KW
+    for box in [(0, 0, 10, T, H, 7), (1, 0, 0, T, H, W), (-1, 0, 0, 2, H, W), (0, 0, 0, 0, H, W),
+                (0, 8, 0, T, 1, W), (0, 0, 0, T, H, 17)]:
+        assert call_region(lib, ptrs, box) == ERR_SHAPE, box
+    # the window is checked against the grid, not the box
+    assert call_region(lib, ptrs, (0, 0, 0, T, H, 3), kernel=(3, 5, 17)) == ERR_KERNEL
+    # empty batch: nothing to do, pointers not looked at
+    assert call_region(lib, (0, 0, 0, 0), (0, 0, 4, T, H, 4), dims=(0, T, H, W, 2, 32)) == OK
+    # out overlapping k, which spans the whole grid
+    n_kv = 1 * T * H * W * 2 * 32 * 2
+    assert call_region(lib, (base, base + (1 << 22), base + (2 << 22), base + (1 << 22) + n_kv // 2),
+                       (0, 0, 0, 2, 2, 2)) == ERR_ALIAS
+
+
 def test_empty_problem_is_a_no_op(lib):
     assert call_fwd(lib, (16, 32, 48, 64), dims=(0, 4, 8, 16, 2, 32)) == OK
     assert call_fwd(lib, (16, 32, 48, 64), dims=(1, 4, 8, 16, 0, 32)) == OK
