@@ -312,6 +312,21 @@ int na3d_fwd_region(const void* q, const void* k, const void* v, void* out, int6
     kp.div_cr = na3d::make_fastdiv(kp.cr);
     kp.div_cw = na3d::make_fastdiv(kp.cw);
 
+    // Head groups: the largest power of two dividing NH whose groups still
+    // fill the persistent grid within 3 % of the best balance.
+    const int64_t slots = int64_t(sms) * vi.ctas_per_sm;   // persistent CTAs
+    auto balance = [&](int64_t hg) {
+        const int64_t groups = units / hg;
+        const int64_t waves = (groups + slots - 1) / slots;
+        return double(groups) / double(waves * slots);
+    };
+    double best = 0;
+    for (int64_t d = 1; d <= NH; d *= 2)
+        if (NH % d == 0 && balance(d) > best) best = balance(d);
+    kp.hg = 1;
+    for (int64_t d = 1; HD >= 128 && d <= NH; d *= 2)   // the kernel groups heads for HD >= 128
+        if (NH % d == 0 && balance(d) >= best - 0.03) kp.hg = int32_t(d);
+
     // Q over the query box, K and V over the whole grid
     CUtensorMap tq, tk, tv;
     if (!encode_map(&tq, q, B, Tq, Hq, Wq, NH, HD, q_token_stride, vi.hd_box, pl.bw, pl.bh, pl.bt) ||
@@ -319,8 +334,8 @@ int na3d_fwd_region(const void* q, const void* k, const void* v, void* out, int6
         !encode_map(&tv, v, B, T, H, W, NH, HD, v_token_stride, vi.hd_box, pl.cw, pl.cr, 1))
         return NA3D_ERR_CUDA;
 
-    const int64_t slots = int64_t(sms) * vi.ctas_per_sm;   // persistent CTAs
-    const int grid = int(units < slots ? units : slots);
+    const int64_t groups = units / kp.hg;
+    const int grid = int(groups < slots ? groups : slots);
     if (na3d::launch_fwd(int(HD), pl.cwp, tq, tk, tv, kp, grid, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return NA3D_ERR_CUDA;

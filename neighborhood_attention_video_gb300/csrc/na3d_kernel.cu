@@ -101,6 +101,10 @@ struct Cfg {
     // next tile goes to other columns and is issued before the softmax has
     // read the current one
     static constexpr int SLAG = STEP == 1 ? 1 : RING;
+    // Head groups (several heads of one brick back to back) pay for HD >= 128,
+    // where a unit boundary is a large share of a unit; smaller HD keeps the
+    // plain round-robin unit order (and its smaller code).
+    static constexpr bool GROUPED = HD >= 128;
     // first slot of chunk g's score tile (and of its P)
     static __device__ __forceinline__ uint32_t slot_of(uint32_t g) { return (g * STEP) % NSLOT; }
     // Shared memory: double-buffer Q and Qx where the per-SM share allows it.
@@ -191,6 +195,28 @@ __device__ __forceinline__ Unit unit_of(const KernelParams& p, int u) {
     return U;
 }
 
+// Unit order of a CTA: the hg heads of one brick back to back (one head group),
+// then the group gridDim.x groups further on. Neighbouring CTAs work on
+// neighbouring bricks at the same head, so their halos meet in L2, and the
+// per-brick work (W masks, row set-up) is done once per group.
+// Instances without head groups (hg = 1) use u, u + gridDim.x, ...
+template <class C>
+__device__ __forceinline__ int first_unit(const KernelParams& p) {
+    if constexpr (C::GROUPED) return blockIdx.x * p.hg;
+    else return blockIdx.x;
+}
+template <class C>
+__device__ __forceinline__ bool group_end(const KernelParams& p, int u) {
+    if constexpr (C::GROUPED) return ((u + 1) & (p.hg - 1)) == 0;
+    else return true;
+}
+template <class C>
+__device__ __forceinline__ int next_unit(const KernelParams& p, int u) {
+    if constexpr (C::GROUPED)
+        return group_end<C>(p, u) ? u + 1 + (static_cast<int>(gridDim.x) - 1) * p.hg : u + 1;
+    else return u + static_cast<int>(gridDim.x);
+}
+
 // Chunk order inside a unit: w-segment fastest, then h-row group, then frame.
 struct ChunkCursor {
     int kt, hc, wc;
@@ -272,7 +298,7 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tq, cons
 
     bool ok = true;
     uint32_t ul = 0;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++ul) {
+    for (int u = first_unit<C>(p); ok && u < p.n_units; u = next_unit<C>(p, u), ++ul) {
         const Unit U = unit_of(p, u);
         const int xq = U.n * C::HD;
         ChunkCursor cur{U.lo_t, 0, 0};
@@ -321,16 +347,20 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tq, cons
 
 // ------------------------------------------------------------------ tensor-core issuer
 
-// Walks the CTA's chunks in order: unit u (blockIdx.x, += gridDim.x), chunk c.
+// Walks the CTA's chunks in order: unit u (see next_unit), chunk c.
 // The unit's chunk count is decoded once, at its first chunk (one call site).
+template <class C>
 struct ChunkWalk {
     int u, c, nch;
-    uint32_t ul, g;   // local unit counter, global chunk counter
+    uint32_t ul, g, gl;   // local unit, global chunk and local head-group counters
+    bool gfirst;          // the unit opens its head group
     __device__ __forceinline__ void start(const KernelParams& p) {
-        u = blockIdx.x;
+        u = first_unit<C>(p);
         c = 0;
         ul = 0;
         g = 0;
+        gl = 0;
+        gfirst = true;
         nch = 0;
     }
     // false when the CTA has no units left; decodes a new unit's chunk count
@@ -339,12 +369,14 @@ struct ChunkWalk {
         if (c == 0) nch = unit_of(p, u).nch;
         return true;
     }
-    __device__ __forceinline__ void next() {
+    __device__ __forceinline__ void next(const KernelParams& p) {
         ++g;
         if (++c == nch) {
             c = 0;
             ++ul;
-            u += gridDim.x;
+            gfirst = group_end<C>(p, u);
+            if (gfirst) ++gl;
+            u = next_unit<C>(p, u);
         }
     }
 };
@@ -390,15 +422,15 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
                 umma_ss_halves<1>(d, x_lo + kk * 2, x_hi, y_l + kk * 2, x_hi, idesc);
         }
     };
-    ChunkWalk w;
+    ChunkWalk<C> w;
     w.start(p);
     while (w.more(p)) {
         const uint32_t qb = w.ul % C::NQ, st = w.g % C::NS;
         if (w.c == 0 && !sy.wait(sy.bar(C::B_QFULL + qb), (w.ul / C::NQ) & 1u)) break;
         uint32_t xb = 0;
         if constexpr (C::FAST) {
-            xb = w.ul % C::NQX;
-            if (w.c == 0 && !sy.wait(sy.bar(C::B_XFULL + xb), (w.ul / C::NQX) & 1u)) break;
+            xb = w.gl % C::NQX;   // one W-mask tile per head group
+            if (w.c == 0 && w.gfirst && !sy.wait(sy.bar(C::B_XFULL + xb), (w.gl / C::NQX) & 1u)) break;
         }
         if (!sy.wait(sy.bar(C::B_KFULL + st), (w.g / C::NS) & 1u)) break;
         // the tile that last used these columns has been read, and the
@@ -429,9 +461,11 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
         umma_commit(sy.bar(C::B_KEMPTY + st));
         if (w.c == w.nch - 1) {
             umma_commit(sy.bar(C::B_QEMPTY + qb));
-            if constexpr (C::FAST) umma_commit(sy.bar(C::B_XEMPTY + xb));
+            if constexpr (C::FAST) {
+                if (group_end<C>(p, w.u)) umma_commit(sy.bar(C::B_XEMPTY + xb));
+            }
         }
-        w.next();
+        w.next(p);
     }
     // Drain: all MMAs issued by this thread complete before TMEM is freed.
     umma_commit(sy.bar(C::B_DRAIN));
@@ -447,7 +481,7 @@ __device__ void mma_pv_role(const KernelParams& p, const Sync& sy, uint32_t base
     const uint64_t vd0 = make_smem_desc(base + C::OFF_V, C::KV_REG, C::SBO, C::SWZ);
     const uint32_t v_hi = static_cast<uint32_t>(vd0 >> 32);
     const int ksteps = p.n_mma >> 4;
-    ChunkWalk w;
+    ChunkWalk<C> w;
     w.start(p);
     while (w.more(p)) {
         const uint32_t st = w.g % C::NS;
@@ -466,7 +500,7 @@ __device__ void mma_pv_role(const KernelParams& p, const Sync& sy, uint32_t base
         umma_commit(sy.bar(C::B_PFREE + w.g % C::RING));
         umma_commit(sy.bar(C::B_VEMPTY + st));
         if (w.c == w.nch - 1) umma_commit(sy.bar(C::B_OFULL));
-        w.next();
+        w.next(p);
     }
     umma_commit(sy.bar(C::B_DRAIN2));
     mbar_wait_bounded(sy.bar(C::B_DRAIN2), 0, kDrainLimitNs);
@@ -615,8 +649,9 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
     const int iw = r % p.bw, ih = (r / p.bw) % p.bh, it = r / (p.bw * p.bh);
     uint32_t g = 0, ul = 0;
 
-    // Qx row of unit X (local index `v`): -2^40 where this row's query does
-    // not see the chunk column, 0 elsewhere; published for the tensor core.
+    // Qx row of the brick of unit X (local head-group index `v`): -2^40 where
+    // this row's query does not see the chunk column, 0 elsewhere; published
+    // for the tensor core once per head group.
     auto publish_qx = [&](uint32_t v, const Unit& X) -> bool {
         if constexpr (C::FAST) {
             const uint32_t xb = v % C::NQX;
@@ -645,8 +680,9 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
         return true;
     };
 
-    int u = blockIdx.x;
-    Unit U{};   // the unit being processed; decoded once, when its W masks go out
+    int u = first_unit<C>(p);
+    uint32_t gl = 0;   // local head-group counter (W-mask tiles)
+    Unit U{};          // the unit being processed, decoded when the previous one ends
     if (u < p.n_units) {
         U = unit_of(p, u);
         if (!publish_qx(0, U)) return;
@@ -658,7 +694,7 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
     uint32_t e_ul = 0;
     bool e_valid = false, e_live = false;
 
-    for (;; u += gridDim.x, ++ul) {
+    for (;; ++ul) {
         const bool have = u < p.n_units;
         const int t = U.t0 + it, h = U.h0 + ih, w = U.w0 + iw;
         const bool valid = have && r < M && t < p.Tq && h < p.Hq && w < p.Wq;
@@ -852,9 +888,15 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
         e_ul = ul;
         e_valid = valid;
         e_live = true;
-        if (u + static_cast<int>(gridDim.x) < p.n_units) {
-            U = unit_of(p, u + gridDim.x);
-            if (!publish_qx(ul + 1, U)) return;
+        const bool new_group = group_end<C>(p, u);
+        u = next_unit<C>(p, u);
+        if (u < p.n_units) {
+            if (new_group) {   // another brick: decode it and publish its W masks
+                U = unit_of(p, u);
+                if (!publish_qx(++gl, U)) return;
+            } else {           // the next head of the same brick
+                ++U.n;
+            }
         }
     }
 }

@@ -35,7 +35,9 @@ struct KernelParams {
     int32_t bt, bh, bw;      // query brick
     int32_t nbt, nbh, nbw;   // bricks per axis of the query box
     int32_t cw, cr, n_mma;   // chunk geometry and score-tile width
-    int32_t n_units;         // B * nbt * nbh * nbw * NH
+    int32_t n_units;         // B * nbt * nbh * nbw * NH (head fastest)
+    int32_t hg;              // heads per group (a power of two dividing NH): a CTA runs the
+                             // hg heads of one brick back to back (1 for HD < 128)
     uint16_t* out;           // bf16 output, (B,Tq,Hq,Wq,NH,HD)
     int32_t out_v8;          // 1: out is 32-byte aligned (32-byte stores), 0: 16-byte stores
     FastDiv div_nh, div_nbw, div_nbh, div_nbt;   // unit index decomposition
