@@ -449,9 +449,24 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
         const uint32_t x_lo = C::FAST ? x_lo0 + ((xb * C::QX_TILE) >> 4) : 0u;
         const uint32_t slot = C::slot_of(w.g);
         const uint32_t d = tmem + C::TM_R + slot * C::SW;
-        if (C::STEP == 1 && slot + 1 == static_cast<uint32_t>(C::NSLOT)) {
+        // A tile that wraps around the ring goes out as two halves, keys SW..
+        // to the first slot. With the tensor-core W mask one copy of the MMA
+        // sequence serves both (smaller code measured faster there); the
+        // per-key-mask instances measured faster with the halves written out.
+        const bool wrap = C::STEP == 1 && slot + 1 == static_cast<uint32_t>(C::NSLOT);
+        if constexpr (C::FAST) {
+            const int halves = wrap && n_hi > 0 ? 2 : 1;
+#pragma unroll 1
+            for (int hh = 0; hh < halves; ++hh) {
+                const uint32_t dd = hh == 0 ? d : tmem + C::TM_R;
+                const uint32_t kl = hh == 0 ? k_lo : k_lo + ((C::SW * C::ROWB) >> 4);
+                const uint32_t yl = hh == 0 ? y_lo : y_lo + ((C::SW * C::XROWB) >> 4);
+                const uint32_t id = !wrap ? idesc_s : (hh == 0 ? idesc_lo : idesc_hi);
+                issue(dd, q_lo, kl, x_lo, yl, id);
+            }
+        } else if (wrap) {
             issue(d, q_lo, k_lo, x_lo, y_lo, idesc_lo);
-            if (n_hi > 0)   // keys SW.. go to the first slot of the ring
+            if (n_hi > 0)
                 issue(tmem + C::TM_R, q_lo, k_lo + ((C::SW * C::ROWB) >> 4), x_lo,
                       y_lo + ((C::SW * C::XROWB) >> 4), idesc_hi);
         } else {
