@@ -53,6 +53,12 @@ WORKLOADS = {
     "na3d_b2_t8_h64_w33_nh8_hd64_k3x7x33": ((2, 8, 64, 33, 8, 64), (3, 7, 33)),
 }
 HEADLINE = "na3d_b1_t16_h64_w64_nh8_hd64_k3x7x7"
+# Smaller cases of the same kernel instances for ncu captures (inputs still
+# larger than L2); selectable with --workload, not part of the configs table.
+PROFILE_WORKLOADS = {
+    "na3d_b1_t16_h48_w64_nh16_hd128_k3x7x7": ((1, 16, 48, 64, 16, 128), (3, 7, 7)),
+}
+ALL_WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS}
 
 
 def useful_flops(shape, kernel):
@@ -241,7 +247,7 @@ def run_ours(args):
 
     world, rank, local, pg = dist_setup(args)
     peaks, peak_src = load_peaks()
-    shape, kernel = WORKLOADS[args.workload]
+    shape, kernel = ALL_WORKLOADS[args.workload]
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
 
@@ -437,7 +443,7 @@ def run_reference(args):
 
     import na3d_inputs
     import oracle
-    shape, kernel = WORKLOADS[args.workload]
+    shape, kernel = ALL_WORKLOADS[args.workload]
     cores = os.cpu_count() or 1
     q, k, v = na3d_inputs.make_qkv(*shape, seed=args.seed)
     total = int(np.prod(shape[:5]))
@@ -480,7 +486,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
+    ap.add_argument("--workload", choices=sorted(ALL_WORKLOADS), default=HEADLINE)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-configs", action="store_true")
