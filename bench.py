@@ -410,18 +410,17 @@ def oracle_sample_rate(shape, kernel, seed, budget_s, nthreads):
     total = int(np.prod(shape[:5]))
     per_row = 4.0 * shape[5] * kernel[0] * kernel[1] * kernel[2]
     rng = np.random.default_rng(seed)
+    # grow the sample until it takes at least half the budget (a small probe
+    # is dominated by fixed costs) or covers the whole workload
     n = min(total, 2048)
-    rows = rng.choice(total, size=n, replace=False)
-    t0 = time.perf_counter()
-    oracle.na3d_fwd_rows(q, k, v, kernel, rows, nthreads=nthreads)
-    dt = time.perf_counter() - t0
-    n2 = int(min(total, max(n, n * budget_s / max(dt, 1e-6))))
-    if n2 > n:
-        rows = rng.choice(total, size=n2, replace=False)
+    for _ in range(5):
+        rows = rng.choice(total, size=n, replace=False)
         t0 = time.perf_counter()
         oracle.na3d_fwd_rows(q, k, v, kernel, rows, nthreads=nthreads)
         dt = time.perf_counter() - t0
-        n = n2
+        if dt >= 0.5 * budget_s or n == total:
+            break
+        n = int(min(total, max(2 * n, 0.9 * n * budget_s / max(dt, 1e-6))))
     return per_row * n / dt / 1e12, n, dt
 
 
