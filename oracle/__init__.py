@@ -125,3 +125,36 @@ def na3d_row_detail(q, k, v, kernel_size, row: int):
     if rc:
         raise ValueError(f"oracle rejected the problem (code {rc})")
     return toks, wts, o
+
+
+# ---------------------------------------------------------------- QKV projection
+
+def _widen_bf16(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> exact fp64 values."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def qkv_projection(x, w, bias, num_heads: int, head_dim: int) -> np.ndarray:
+    """The fused QKV projection in fp64 (test infrastructure).
+
+    x: bf16 bits (M, C); w: bf16 bits (3*NH*HD, C), q rows first, then k,
+    then v; bias: bf16 bits (3*NH*HD,) or None. Returns fp64 (M, 3*NH*HD):
+    x w^T + bias, with the q block (the first NH*HD columns) multiplied by
+    head_dim^-0.5.
+
+    The projection is the one the decoder attention uses: one concatenated
+    Q/K/V weight whose output q, k, v are views of ("LTX-2.5 optimization:
+    integrate faster AITER NA3D flash attention for diffusion decoder", xDiT
+    pull request 773, Summary; Notes); the attention takes q pre-scaled by
+    head_dim^-0.5 ("[Triton/Gluon] Add 3D neighborhood flash attention
+    (na3d_flash)", Technical Details, launcher). A plain matrix product
+    (library routine) on the exactly widened inputs; no blocking.
+    """
+    xf, wf = _widen_bf16(x), _widen_bf16(w)
+    y = xf @ wf.T
+    if bias is not None:
+        y = y + _widen_bf16(bias)[None, :]
+    nq = num_heads * head_dim
+    y[:, :nq] *= head_dim ** -0.5
+    return y
