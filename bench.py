@@ -356,6 +356,7 @@ def run_ours(args):
 
     if rank == 0 and not args.no_configs:
         result["configs"] = per_config_table(dev, stream, flush, peaks)
+        result["qkv_projection"] = projection_line(shape, dev, stream, flush, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(shape, kernel, args.seed, budget_s=args.cpu_seconds)
     if rank == 0:
@@ -395,6 +396,44 @@ def per_config_table(dev, stream, flush, peaks, steps=20, warmup=3):
         del q, k, v, out
     torch.cuda.synchronize()
     return table
+
+
+def projection_line(shape, dev, stream, flush, peaks, steps=20, warmup=3):
+    """The fused QKV projection that produces this workload's q, k, v:
+    x (B*T*H*W tokens, C = NH*HD channels) times a (3*NH*HD, C) weight with
+    a bias; a dense contraction, so its roofline is the bf16 tensor peak."""
+    import torch
+    import neighborhood_attention_video_gb300 as na
+    B, T, H, W, NH, HD = shape
+    M, C, N = B * T * H * W, NH * HD, 3 * NH * HD
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    x = torch.randn((M, C), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    w = (torch.randn((N, C), generator=gen, device=dev, dtype=torch.float32) / math.sqrt(C)).to(torch.bfloat16)
+    bias = torch.randn((N,), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    qkv = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    for _ in range(warmup):
+        na.na3d_qkv_proj(x, w, bias, qkv, NH, HD, stream=stream)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            na.na3d_qkv_proj(x, w, bias, qkv, NH, HD, stream=stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    t = statistics.median(a.elapsed_time(b) * 1e-3 for a, b in evs)
+    flops = 2.0 * M * C * N
+    nbytes = 2.0 * (M * C + N * C + M * N)
+    del x, w, bias, qkv
+    return {
+        "shape_M_C_N": [M, C, N], "us": t * 1e6, "tflops": flops / t / 1e12,
+        "frac_of_bf16_peak": flops / t / 1e12 / peaks["bf16_tflops"],
+        "hbm_gbs": nbytes / t / 1e9,
+        "roofline_us": max(flops / (peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9)) * 1e6,
+    }
 
 
 # ---------------------------------------------------------------- CPU oracle

@@ -129,6 +129,36 @@ int na3d_fwd_region(const void* q, const void* k, const void* v, void* out,
                     int64_t q_token_stride, int64_t k_token_stride, int64_t v_token_stride,
                     void* stream);
 
+/*
+ * na3d_qkv_proj - the fused QKV projection that feeds the attention:
+ *   qkv[m][n] = bf16( s_n * ( sum_c x[m][c] * w[n][c] + bias[n] ) ),
+ *   s_n = HD^-0.5 (rounded to fp32) for n < NH*HD (the q block), else 1,
+ * with the sum and the bias added in fp32 and one rounding to bf16 (nearest
+ * even). The decoder attention of "LTX-2.5 optimization: integrate faster
+ * AITER NA3D flash attention for diffusion decoder" (xDiT pull request 773,
+ * Summary; Notes) projects q, k and v with one concatenated weight and takes
+ * q, k, v as views of the result; the attention wants q already scaled by
+ * HD^-0.5 ("[Triton/Gluon] Add 3D neighborhood flash attention (na3d_flash)",
+ * Technical Details, launcher). A row of qkv is [q heads | k heads | v heads],
+ * i.e. (M, 3, NH, HD): pass qkv, qkv + NH*HD and qkv + 2*NH*HD (elements) to
+ * na3d_fwd_strided with token strides 3*NH*HD, and M = B*T*H*W tokens in
+ * (b, t, h, w) order.
+ *
+ * x: DEVICE pointer, bf16 (M, C) row-major (a token's C input channels).
+ * w: DEVICE pointer, bf16 (3*NH*HD, C) row-major (one output feature per
+ *   row, as a linear layer's weight), q rows first, then k, then v.
+ * bias: DEVICE pointer, bf16 (3*NH*HD), or NULL for none.
+ * qkv: DEVICE pointer, bf16 (M, 3*NH*HD) row-major; must not overlap x, w or
+ *   bias. x, w and qkv are 16-byte aligned; C is a multiple of 8 (16-byte
+ *   rows), else NA3D_ERR_ALIGN.
+ * M >= 0 tokens, NH >= 0 heads (either 0: nothing to do, pointers not
+ *   looked at), C >= 1, HD a power of two >= 16.
+ * Asynchronous on `stream`; errors as for na3d_fwd. na3d_device_status also
+ * reports a pipeline wait of this kernel that gave up.
+ */
+int na3d_qkv_proj(const void* x, const void* w, const void* bias, void* qkv,
+                  int64_t M, int64_t C, int64_t NH, int64_t HD, void* stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* na3d_status_string(int status);
 

@@ -14,14 +14,14 @@ import os
 
 __all__ = [
     "NA3DError", "NA3DUnavailable", "na3d_fwd", "na3d_fwd_strided", "na3d_fwd_region",
-    "na3d_status_string", "na3d_plan",
+    "na3d_qkv_proj", "qkv_views", "na3d_status_string", "na3d_plan",
     "na3d_device_status", "library_path", "load_library", "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libna3d.so")
-EXPORTED_SYMBOLS = ("na3d_fwd", "na3d_fwd_strided", "na3d_fwd_region", "na3d_status_string",
-                    "na3d_plan", "na3d_device_status")
+EXPORTED_SYMBOLS = ("na3d_fwd", "na3d_fwd_strided", "na3d_fwd_region", "na3d_qkv_proj",
+                    "na3d_status_string", "na3d_plan", "na3d_device_status")
 
 NA3D_OK = 0
 _I64 = ctypes.c_int64
@@ -69,6 +69,8 @@ def load_library():
     lib.na3d_fwd_strided.restype = ctypes.c_int
     lib.na3d_fwd_region.argtypes = [_P, _P, _P, _P] + [_I64] * 18 + [_P]
     lib.na3d_fwd_region.restype = ctypes.c_int
+    lib.na3d_qkv_proj.argtypes = [_P, _P, _P, _P] + [_I64] * 4 + [_P]
+    lib.na3d_qkv_proj.restype = ctypes.c_int
     lib.na3d_status_string.argtypes = [ctypes.c_int]
     lib.na3d_status_string.restype = ctypes.c_char_p
     lib.na3d_plan.argtypes = [_I64] * 8 + [ctypes.POINTER(PlanInfo)]
@@ -185,6 +187,40 @@ def na3d_fwd_region(q, k, v, out, kernel_size, offset, stream=None) -> None:
                              *strides, _stream_handle(stream))
     if rc != NA3D_OK:
         raise NA3DError(rc, "na3d_fwd_region")
+
+
+def na3d_qkv_proj(x, w, bias, qkv, num_heads, head_dim, stream=None) -> None:
+    """qkv = x w^T (+ bias), the q block scaled by head_dim**-0.5 (see
+    ``na3d_qkv_proj`` in include/na3d.h). x: contiguous bf16 CUDA tensor
+    (..., C); w: (3*NH*HD, C); bias: (3*NH*HD,) or None; qkv: contiguous bf16
+    with x's leading dimensions and 3*NH*HD elements per token, e.g.
+    (B, T, H, W, 3, NH, HD). ``qkv_views`` gives the attention inputs."""
+    import torch
+    lib = load_library()
+    tensors = [("x", x), ("w", w), ("qkv", qkv)] + ([("bias", bias)] if bias is not None else [])
+    for name, t in tensors:
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+    NH, HD = int(num_heads), int(head_dim)
+    C = int(x.shape[-1])
+    M = x.numel() // C if C else 0
+    N = 3 * NH * HD
+    if tuple(w.shape) != (N, C) or (bias is not None and tuple(bias.shape) != (N,)):
+        raise ValueError("w must be (3*NH*HD, C) and bias (3*NH*HD,)")
+    if qkv.numel() != M * N:
+        raise ValueError("qkv must hold 3*NH*HD values per token of x")
+    rc = lib.na3d_qkv_proj(x.data_ptr(), w.data_ptr(), bias.data_ptr() if bias is not None else None,
+                           qkv.data_ptr(), M, C, NH, HD, _stream_handle(stream))
+    if rc != NA3D_OK:
+        raise NA3DError(rc, "na3d_qkv_proj")
+
+
+def qkv_views(qkv):
+    """q, k, v views (B, T, H, W, NH, HD) of a (B, T, H, W, 3, NH, HD)
+    projection output, for ``na3d_fwd_strided``."""
+    return qkv[..., 0, :, :], qkv[..., 1, :, :], qkv[..., 2, :, :]
 
 
 def na3d_plan(T, H, W, NH, HD, KT, KH, KW) -> dict:

@@ -1,6 +1,6 @@
 """Build the in-tree CUDA library ``libna3d.so`` for sm_103a (nvcc, no cmake).
 
-The two translation units compile in parallel, then link with the static
+The translation units compile in parallel, then link with the static
 CUDA runtime, so the library loads on machines without a GPU or a shared
 libcudart (it reaches the driver only when a CUDA call is made).
 """
@@ -17,8 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libna3d.so")
-SOURCES = ["na3d_kernel.cu", "na3d_api.cu"]
-DEPS = SOURCES + ["na3d_kernel.cuh", "sm103_ptx.cuh"]
+SOURCES = ["na3d_kernel.cu", "na3d_proj.cu", "na3d_api.cu"]
+DEPS = SOURCES + ["na3d_kernel.cuh", "na3d_proj.cuh", "sm103_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -11,6 +11,7 @@
 
 #include "na3d.h"
 #include "na3d_kernel.cuh"
+#include "na3d_proj.cuh"
 
 namespace {
 
@@ -195,6 +196,21 @@ bool encode_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t H
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A row-major (outer, inner) bf16 matrix as a 2-D tensor map with a
+// (box_inner, box_outer) box and the 128-byte swizzle (box_inner = 64).
+bool encode_map_2d(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int box_inner,
+                   int box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+    const cuuint64_t strides[1] = {cuuint64_t(inner * 2)};
+    const cuuint32_t box[2] = {cuuint32_t(box_inner), cuuint32_t(box_outer)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Do the byte ranges [a, a + a_bytes) and [b, b + b_bytes) intersect?
 bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -357,11 +373,63 @@ int na3d_fwd(const void* q, const void* k, const void* v, void* out, int64_t B, 
                             NH * HD, stream);
 }
 
-int na3d_device_status(void* stream) {
-    unsigned int flag = 0;
-    if (na3d::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &flag) != cudaSuccess)
+int na3d_qkv_proj(const void* x, const void* w, const void* bias, void* qkv, int64_t M, int64_t C,
+                  int64_t NH, int64_t HD, void* stream) {
+    if (M < 0 || NH < 0 || C < 1 || HD < 1) return NA3D_ERR_SHAPE;
+    if (!is_pow2(HD) || HD < 16) return NA3D_ERR_HEAD_DIM;
+    if (C % 8 != 0) return NA3D_ERR_ALIGN;   // rows of x and W must be 16-byte aligned
+    int64_t N, xb, wb, ob;
+    if (!mul_ok(3 * NH, HD, &N) || !mul_ok(M, C, &xb) || !mul_ok(xb, 2, &xb) || !mul_ok(N, C, &wb) ||
+        !mul_ok(wb, 2, &wb) || !mul_ok(M, N, &ob) || !mul_ok(ob, 2, &ob))
+        return NA3D_ERR_OVERFLOW;
+    if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || C >= (int64_t(1) << 31))
+        return NA3D_ERR_OVERFLOW;
+    if (ob == 0) return NA3D_OK;   // no tokens or no heads: nothing to write
+    if (!x || !w || !qkv) return NA3D_ERR_NULL;
+    const void* ptrs[3] = {x, w, qkv};
+    for (const void* p : ptrs)
+        if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return NA3D_ERR_ALIGN;
+    if (bias && reinterpret_cast<uintptr_t>(bias) % 2 != 0) return NA3D_ERR_ALIGN;
+    if (overlaps(qkv, ob, x, xb) || overlaps(qkv, ob, w, wb) || (bias && overlaps(qkv, ob, bias, N * 2)))
+        return NA3D_ERR_ALIAS;
+
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return NA3D_ERR_CUDA;
-    return flag ? NA3D_ERR_DEVICE_TIMEOUT : NA3D_OK;
+    if (major != 10 || minor != 3) return NA3D_ERR_ARCH;
+
+    na3d::ProjParams pp;
+    pp.M = int32_t(M);
+    pp.C = int32_t(C);
+    pp.N = int32_t(N);
+    pp.Nq = int32_t(NH * HD);
+    pp.n_tiles_n = int32_t((N + 255) / 256);
+    const int64_t tiles = ((M + 127) / 128) * pp.n_tiles_n;
+    if (tiles >= (int64_t(1) << 31)) return NA3D_ERR_OVERFLOW;
+    pp.n_tiles = int32_t(tiles);
+    pp.k_blocks = int32_t((C + 63) / 64);
+    pp.out_v8 = (reinterpret_cast<uintptr_t>(qkv) % 32u) == 0u ? 1 : 0;   // rows: N * 2 = 96k bytes
+    pp.q_scale = float(1.0 / __builtin_sqrt(double(HD)));
+    pp.bias = static_cast<const uint16_t*>(bias);
+    pp.qkv = static_cast<uint16_t*>(qkv);
+    CUtensorMap tx, tw;
+    if (!encode_map_2d(&tx, x, C, M, 64, 128) || !encode_map_2d(&tw, w, C, N, 64, 256))
+        return NA3D_ERR_CUDA;
+    const int grid = int(tiles < sms ? tiles : sms);
+    if (na3d::launch_qkv_proj(tx, tw, pp, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return NA3D_ERR_CUDA;
+    return NA3D_OK;
+}
+
+int na3d_device_status(void* stream) {
+    unsigned int flag = 0, pflag = 0;
+    if (na3d::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &flag) != cudaSuccess ||
+        na3d::read_and_clear_proj_error(static_cast<cudaStream_t>(stream), &pflag) != cudaSuccess)
+        return NA3D_ERR_CUDA;
+    return (flag || pflag) ? NA3D_ERR_DEVICE_TIMEOUT : NA3D_OK;
 }
 
 }  // extern "C"

@@ -134,6 +134,25 @@ def test_region_validation(lib):
                        (0, 0, 0, 2, 2, 2)) == ERR_ALIAS
 
 
+def test_qkv_proj_validation(lib):
+    import torch
+    expect = OK if torch.cuda.is_available() else ERR_CUDA
+    base = 1 << 20
+    x, w, qkv = base, base + (1 << 24), base + (2 << 24)
+    P = ctypes.c_void_p
+    call = lambda x_, w_, b_, o_, M, C, NH, HD: lib.na3d_qkv_proj(P(x_), P(w_), P(b_), P(o_), M, C,  # noqa: E731
+                                                                    NH, HD, None)
+    assert call(x, w, None, qkv, 1000, 64, 2, 32) == expect
+    assert call(x, w, None, qkv, 1000, 60, 2, 32) == ERR_ALIGN    # rows of 120 bytes
+    assert call(x, w, None, qkv, 1000, 64, 2, 48) == ERR_HEAD_DIM
+    assert call(x, w, None, qkv, -1, 64, 2, 32) == ERR_SHAPE
+    assert call(0, 0, None, 0, 0, 64, 2, 32) == OK                  # no tokens: nothing to do
+    assert call(0, w, None, qkv, 10, 64, 2, 32) == ERR_NULL
+    assert call(x + 8, w, None, qkv, 10, 64, 2, 32) == ERR_ALIGN
+    assert call(x, w, None, x + 64, 10, 64, 2, 32) == ERR_ALIAS   # qkv over x
+    assert call(x, w, qkv + 64, qkv, 10, 64, 2, 32) == ERR_ALIAS  # bias inside qkv
+
+
 def test_empty_problem_is_a_no_op(lib):
     assert call_fwd(lib, (16, 32, 48, 64), dims=(0, 4, 8, 16, 2, 32)) == OK
     assert call_fwd(lib, (16, 32, 48, 64), dims=(1, 4, 8, 16, 0, 32)) == OK
