@@ -106,26 +106,32 @@ Plan make_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap) {
         const int64_t sw = axis_sum(aw, bw, cw, &nbw);
         for (int64_t bh = 1; bh <= ah.nq && bw * bh <= 128; ++bh) {
             const int64_t eh = (bh + KH - 1 < H) ? bh + KH - 1 : H;
-            int64_t cr = (!cwp && ew > ncap) ? 1 : ncap / cw;
-            if (cr > eh) cr = eh;
-            const int64_t n_mma = (cr * cw + 15) / 16 * 16;
-            int64_t nbh;
-            const int64_t sh = axis_sum(ah, bh, cr, &nbh);
-            for (int64_t bt = 1; bt <= at.nq && bw * bh * bt <= 128; ++bt) {
-                int64_t nbt;
-                const int64_t st = axis_sum(at, bt, 1, &nbt);
-                const int64_t chunks = st * sh * sw;
-                const int64_t bricks = nbt * nbh * nbw;
-                const double cost = double(chunks) * (double(n_mma) * col_cost + kChunkOverhead) +
-                                    double(bricks) * kBrickOverhead;
-                const bool better =
-                    best.bt == 0 || cost < best.cost - 1e-9 ||
-                    (cost < best.cost + 1e-9 && bw * bh * bt > int64_t(best.bw) * best.bh * best.bt);
-                if (better) {
-                    best.bt = int(bt); best.bh = int(bh); best.bw = int(bw);
-                    best.cw = int(cw); best.cr = int(cr); best.n_mma = int(n_mma);
-                    best.cwp = int(cwp);
-                    best.bricks = bricks; best.chunks = chunks; best.cost = cost;
+            int64_t cr_max = (!cwp && ew > ncap) ? 1 : ncap / cw;
+            if (cr_max > eh) cr_max = eh;
+            // any row count up to the cap (fewer rows can mean fewer 32-key words)
+            for (int64_t cr = cr_max; cr >= 1; --cr) {
+                const int64_t n_mma = (cr * cw + 15) / 16 * 16;
+                int64_t nbh;
+                const int64_t sh = axis_sum(ah, bh, cr, &nbh);
+                for (int64_t bt = 1; bt <= at.nq && bw * bh * bt <= 128; ++bt) {
+                    int64_t nbt;
+                    const int64_t st = axis_sum(at, bt, 1, &nbt);
+                    const int64_t chunks = st * sh * sw;
+                    const int64_t bricks = nbt * nbh * nbw;
+                    // the softmax works in 32-key words, so a tile costs its width
+                    // rounded up to a word
+                    const int64_t n_words = (n_mma + 31) / 32 * 32;
+                    const double cost = double(chunks) * (double(n_words) * col_cost + kChunkOverhead) +
+                                        double(bricks) * kBrickOverhead;
+                    const bool better =
+                        best.bt == 0 || cost < best.cost - 1e-9 ||
+                        (cost < best.cost + 1e-9 && bw * bh * bt > int64_t(best.bw) * best.bh * best.bt);
+                    if (better) {
+                        best.bt = int(bt); best.bh = int(bh); best.bw = int(bw);
+                        best.cw = int(cw); best.cr = int(cr); best.n_mma = int(n_mma);
+                        best.cwp = int(cwp);
+                        best.bricks = bricks; best.chunks = chunks; best.cost = cost;
+                    }
                 }
             }
         }
