@@ -159,6 +159,21 @@ int na3d_fwd_region(const void* q, const void* k, const void* v, void* out,
 int na3d_qkv_proj(const void* x, const void* w, const void* bias, void* qkv,
                   int64_t M, int64_t C, int64_t NH, int64_t HD, void* stream);
 
+/*
+ * na3d_selftest_withhold - a self-test of the kernel's failure detection:
+ * na3d_fwd on contiguous tensors, except that CTA 0 does not issue the load
+ * of its K chunk number `chunk` (0-based, in its own order). The score-tile
+ * wait for that chunk runs out after about 2 s; the CTA then records the
+ * timeout, drains its in-flight copies and MMAs, frees its tensor memory and
+ * exits, and na3d_device_status() returns NA3D_ERR_DEVICE_TIMEOUT. out is
+ * left partly unwritten. The stream and the device stay usable. Not for
+ * production use. chunk < 0 returns NA3D_ERR_SHAPE; other arguments and
+ * errors as na3d_fwd.
+ */
+int na3d_selftest_withhold(const void* q, const void* k, const void* v, void* out,
+                           int64_t B, int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD,
+                           int64_t KT, int64_t KH, int64_t KW, int64_t chunk, void* stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* na3d_status_string(int status);
 

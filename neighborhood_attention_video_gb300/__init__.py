@@ -21,7 +21,8 @@ __all__ = [
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libna3d.so")
 EXPORTED_SYMBOLS = ("na3d_fwd", "na3d_fwd_strided", "na3d_fwd_region", "na3d_qkv_proj",
-                    "na3d_status_string", "na3d_plan", "na3d_device_status")
+                    "na3d_selftest_withhold", "na3d_status_string", "na3d_plan",
+                    "na3d_device_status")
 
 NA3D_OK = 0
 _I64 = ctypes.c_int64
@@ -71,6 +72,8 @@ def load_library():
     lib.na3d_fwd_region.restype = ctypes.c_int
     lib.na3d_qkv_proj.argtypes = [_P, _P, _P, _P] + [_I64] * 4 + [_P]
     lib.na3d_qkv_proj.restype = ctypes.c_int
+    lib.na3d_selftest_withhold.argtypes = [_P, _P, _P, _P] + [_I64] * 10 + [_P]
+    lib.na3d_selftest_withhold.restype = ctypes.c_int
     lib.na3d_status_string.argtypes = [ctypes.c_int]
     lib.na3d_status_string.restype = ctypes.c_char_p
     lib.na3d_plan.argtypes = [_I64] * 8 + [ctypes.POINTER(PlanInfo)]

@@ -264,11 +264,15 @@ int na3d_plan(int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t K
     return NA3D_OK;
 }
 
-int na3d_fwd_region(const void* q, const void* k, const void* v, void* out, int64_t B, int64_t T,
-                    int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT, int64_t KH, int64_t KW,
-                    int64_t t0, int64_t h0, int64_t w0, int64_t Tq, int64_t Hq, int64_t Wq,
-                    int64_t q_token_stride, int64_t k_token_stride, int64_t v_token_stride,
-                    void* stream) {
+}  // extern "C"
+
+namespace {
+
+int fwd_region(const void* q, const void* k, const void* v, void* out, int64_t B, int64_t T,
+               int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT, int64_t KH, int64_t KW,
+               int64_t t0, int64_t h0, int64_t w0, int64_t Tq, int64_t Hq, int64_t Wq,
+               int64_t q_token_stride, int64_t k_token_stride, int64_t v_token_stride, void* stream,
+               int32_t withhold_k) {
     int rc = validate_shape(B, T, H, W, NH, HD, KT, KH, KW);
     if (rc != NA3D_OK) return rc;
     // the query box lies inside the grid
@@ -327,6 +331,7 @@ int na3d_fwd_region(const void* q, const void* k, const void* v, void* out, int6
     kp.out = static_cast<uint16_t*>(out);
     // rows are HD * 2 >= 32 bytes: 32-byte stores when the base allows them
     kp.out_v8 = (reinterpret_cast<uintptr_t>(out) % 32u) == 0u ? 1 : 0;
+    kp.withhold_k = withhold_k;
     kp.div_nh = na3d::make_fastdiv(kp.NH);
     kp.div_nbw = na3d::make_fastdiv(kp.nbw);
     kp.div_nbh = na3d::make_fastdiv(kp.nbh);
@@ -362,6 +367,27 @@ int na3d_fwd_region(const void* q, const void* k, const void* v, void* out, int6
         cudaSuccess)
         return NA3D_ERR_CUDA;
     return NA3D_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int na3d_fwd_region(const void* q, const void* k, const void* v, void* out, int64_t B, int64_t T,
+                    int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT, int64_t KH, int64_t KW,
+                    int64_t t0, int64_t h0, int64_t w0, int64_t Tq, int64_t Hq, int64_t Wq,
+                    int64_t q_token_stride, int64_t k_token_stride, int64_t v_token_stride,
+                    void* stream) {
+    return fwd_region(q, k, v, out, B, T, H, W, NH, HD, KT, KH, KW, t0, h0, w0, Tq, Hq, Wq,
+                      q_token_stride, k_token_stride, v_token_stride, stream, -1);
+}
+
+int na3d_selftest_withhold(const void* q, const void* k, const void* v, void* out, int64_t B,
+                           int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT,
+                           int64_t KH, int64_t KW, int64_t chunk, void* stream) {
+    if (chunk < 0 || chunk >= (int64_t(1) << 30)) return NA3D_ERR_SHAPE;
+    return fwd_region(q, k, v, out, B, T, H, W, NH, HD, KT, KH, KW, 0, 0, 0, T, H, W, NH * HD,
+                      NH * HD, NH * HD, stream, int32_t(chunk));
 }
 
 int na3d_fwd_strided(const void* q, const void* k, const void* v, void* out, int64_t B, int64_t T,

@@ -308,11 +308,15 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tq, cons
             const uint32_t st = gk % C::NS;
             if (!sy.wait(sy.bar(C::B_KEMPTY + st), ((gk / C::NS) & 1u) ^ 1u)) { ok = false; break; }
             const uint32_t full = sy.bar(C::B_KFULL + st);
-            mbar_arrive_expect_tx(full, kv_bytes);
+            // self-test of the bounded waits: CTA 0 may withhold one K chunk,
+            // whose barrier then never completes
+            if (blockIdx.x != 0 || static_cast<int>(gk) != p.withhold_k) {
+                mbar_arrive_expect_tx(full, kv_bytes);
 #pragma unroll
-            for (int r = 0; r < C::NREG; ++r)
-                tma_load_5d(base + C::OFF_K + st * C::KV_TILE + r * C::KV_REG, tk, full,
-                            cc.x + r * C::HDB, cc.kw0, cc.kh0, cc.kt, cc.b);
+                for (int r = 0; r < C::NREG; ++r)
+                    tma_load_5d(base + C::OFF_K + st * C::KV_TILE + r * C::KV_REG, tk, full,
+                                cc.x + r * C::HDB, cc.kw0, cc.kh0, cc.kt, cc.b);
+            }
             ++gk;
             // V trails K by one chunk; it goes before the unit's Q brick, whose
             // buffer may still be read by the previous unit's last score tile

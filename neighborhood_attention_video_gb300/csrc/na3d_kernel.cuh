@@ -40,6 +40,7 @@ struct KernelParams {
                              // hg heads of one brick back to back (1 for HD < 128)
     uint16_t* out;           // bf16 output, (B,Tq,Hq,Wq,NH,HD)
     int32_t out_v8;          // 1: out is 32-byte aligned (32-byte stores), 0: 16-byte stores
+    int32_t withhold_k;      // self-test: CTA 0 skips its K load number withhold_k (-1: none)
     FastDiv div_nh, div_nbw, div_nbh, div_nbt;   // unit index decomposition
     FastDiv div_cr, div_cw;                      // chunks per halo row group / W segment
 };
