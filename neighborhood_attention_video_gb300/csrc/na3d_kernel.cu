@@ -8,11 +8,14 @@
 // exponent; the output is bf16 in the input layout.
 //
 // Work decomposition. One work unit is one query brick (bt x bh x bw <= 128
-// grid positions) of one (batch, head). Its keys are the union of its
-// queries' windows (the halo), a box that is streamed through shared memory
-// in chunks: a chunk is cr consecutive rows (h) of cw consecutive keys (w) in
-// one frame (t), loaded with one TMA box per 64 head-dim columns. Queries are
-// the M = 128 rows of every tensor-core tile; a chunk's keys are its N columns.
+// grid positions of the query box, which is the whole grid unless a region is
+// given) of one (batch, head). Its keys are the union of its queries' windows
+// (the halo, in grid coordinates), a box that is streamed through shared
+// memory in chunks: a chunk is cr consecutive rows (h) of cw consecutive keys
+// (w) in one frame (t), loaded with one TMA box per 64 head-dim columns.
+// Queries are the M = 128 rows of every tensor-core tile; a chunk's keys are
+// its N columns. Persistent CTAs take units round-robin; for HD >= 128 a CTA
+// takes the heads of one brick back to back (see next_unit).
 //
 // Roles (256 threads; two CTAs per SM for HD <= 128, one for HD = 256):
 //   warps 0..3  softmax (warpgroup 0): one query row per thread (its TMEM
@@ -900,7 +903,8 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
             mbar_arrive(sy.bar(C::B_PFULL + g % C::RING));
         }
 
-        // the next unit's W masks go out before this unit's epilogue
+        // this unit's output is written at the top of the next iteration, once
+        // the next unit is set up; its W masks go out now
         const int64_t tok = ((static_cast<int64_t>(U.b) * p.Tq + t) * p.Hq + h) * p.Wq + w;
         e_orow = p.out + (tok * p.NH + U.n) * C::HD;
         e_l = l;
