@@ -59,6 +59,8 @@ FULL_CASES = [
     ((1, 4, 8, 16, 2, 32), (3, 5, 5)),       # the tiny benchmark configuration, seed 0
     ((1, 6, 20, 36, 2, 64), (3, 7, 7)),      # several bricks, ragged tails on every axis
     ((2, 5, 13, 19, 3, 128), (3, 5, 7)),     # HD 128, B and NH > 1, ragged
+    ((1, 3, 6, 40, 2, 128), (3, 5, 33)),     # HD 128 with per-key masks (W union over 32 keys)
+    ((1, 8, 14, 14, 4, 128), (7, 9, 9)),     # HD 128, many chunks per unit, head groups
     ((1, 4, 9, 40, 2, 256), (3, 3, 11)),     # HD 256 (64-key chunks)
     ((1, 3, 7, 11, 2, 16), (3, 5, 5)),       # HD 16
     ((1, 16, 64, 5, 8, 64), (3, 5, 5)),      # narrow edge tile: W = KW = 5
@@ -148,13 +150,15 @@ def test_axis_flip_equivariance():
         assert rel < 5e-3, (axis, rel)
 
 
+@pytest.mark.parametrize("hd", [64, 128])
 @pytest.mark.parametrize("kernel", [(3, 5, 7), (3, 7, 33)], ids=lambda x: "x".join(map(str, x)))
-def test_score_spike_in_a_later_chunk(kernel):
+def test_score_spike_in_a_later_chunk(kernel, hd):
     """Keys of the last frames are scaled up, so rows meet scores tens of log2
     units above everything they saw in earlier chunks: the kept reference
     maximum must be raised mid-row and O rescaled (the exact pass taken when a
-    chunk's probabilities sum past 2^32)."""
-    shape = (1, 6, 12, 36, 2, 64)
+    chunk's probabilities sum past 2^32). With HD 128 the two halves of each
+    score row must take these steps together."""
+    shape = (1, 6, 12, 36, 2, hd)
     q, k, v = na3d_inputs.make_qkv(*shape, seed=13)
     kf = na3d_inputs.bf16_bits_to_f64(k)
     kf[:, 4:] *= 40.0
@@ -226,12 +230,13 @@ def test_empty_batch_is_a_no_op():
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("hd", [64, 128])
 @pytest.mark.parametrize("shift", [0, 8], ids=["out32B", "out16B"])
-def test_output_untouched_outside_the_tensor(shift):
+def test_output_untouched_outside_the_tensor(shift, hd):
     """The kernel writes exactly the output tensor: guard bands around it keep
     their sentinel values. `shift` elements move the output off a 32-byte
     boundary (16-byte stores instead of 32-byte ones)."""
-    shape, kernel = (1, 5, 11, 13, 3, 64), (3, 5, 5)
+    shape, kernel = (1, 5, 11, 13, 3, hd), (3, 5, 5)
     q, k, v = na3d_inputs.make_qkv(*shape, seed=5)
     n = int(np.prod(shape))
     guard = 4096 + shift
