@@ -83,9 +83,14 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def roofline_terms(shape, kernel, seconds, peaks):
+# NVIDIA's published dense (no sparsity) bf16 tensor throughput of one GB300
+# GPU, for context beside the measured peaks
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
+def roofline_terms(shape, kernel, seconds, peaks, tc_tflops=None):
     flops, nbytes = useful_flops(shape, kernel), min_bytes(shape)
-    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_tc = flops / ((tc_tflops or peaks["bf16_tflops"]) * 1e12)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
     bound = "tensor" if t_tc >= t_hbm else "hbm"
     return {
@@ -220,7 +225,8 @@ def gpu_uuid(local):
 
 
 def time_kernel(shape, kernel, q, k, v, out, steps, warmup, flush, stream):
-    """Per-step CUDA-event kernel times (s) with the L2 flushed between steps."""
+    """Per-step CUDA-event kernel times (s) with the L2 flushed between steps
+    (flush None: back to back, inputs left in L2 by the previous step)."""
     import torch
     import neighborhood_attention_video_gb300 as na
     for _ in range(warmup):
@@ -230,7 +236,8 @@ def time_kernel(shape, kernel, q, k, v, out, steps, warmup, flush, stream):
            for _ in range(steps)]
     with torch.cuda.stream(stream):
         for a, b in evs:
-            flush.zero_()
+            if flush is not None:
+                flush.zero_()
             a.record(stream)
             na.na3d_fwd(q, k, v, out, kernel, stream=stream)
             b.record(stream)
@@ -359,6 +366,8 @@ def run_ours(args):
         result["qkv_projection"] = projection_line(shape, dev, stream, flush, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(shape, kernel, args.seed, budget_s=args.cpu_seconds)
+        if not args.no_configs:
+            result["cpu_oracle_per_config"] = cpu_per_config(args.seed)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if pg is not None:
@@ -381,7 +390,10 @@ def per_config_table(dev, stream, flush, peaks, steps=20, warmup=3):
         out = torch.empty_like(q)
         times = time_kernel(shape, kernel, q, k, v, out, steps, warmup, flush, stream)
         t = statistics.median(times)
+        t_warm = statistics.median(time_kernel(shape, kernel, q, k, v, out, steps, 1, None, stream))
         terms = roofline_terms(shape, kernel, t, peaks)
+        sustained = roofline_terms(shape, kernel, t, peaks, peaks["bf16_tflops_sustained"])
+        nominal = roofline_terms(shape, kernel, t, peaks, NOMINAL_BF16_TFLOPS)
         plan = na.na3d_plan(*shape[1:], *kernel)
         executed = plan["chunks_per_slice"] * shape[0] * shape[4] * 128 * plan["n_mma"] * shape[5] * 4.0
         table[name] = {
@@ -390,6 +402,9 @@ def per_config_table(dev, stream, flush, peaks, steps=20, warmup=3):
             "roofline_frac": terms["roofline_frac"],
             "bound": terms["bound"],
             "roofline_us": terms["roofline_us"],
+            "roofline_frac_sustained_tc": sustained["roofline_frac"],
+            "roofline_frac_nominal_tc": nominal["roofline_frac"],
+            "us_warm": t_warm * 1e6,
             "executed_tflops": executed / t / 1e12,
             "plan": [plan["bt"], plan["bh"], plan["bw"], plan["cw"], plan["cr"], plan["n_mma"]],
         }
@@ -463,11 +478,59 @@ def oracle_sample_rate(shape, kernel, seed, budget_s, nthreads):
     return per_row * n / dt / 1e12, n, dt
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    import subprocess
+    try:
+        txt = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in txt.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(shape, kernel, seed, budget_s=10.0):
     cores = os.cpu_count() or 1
     tf, n, dt = oracle_sample_rate(shape, kernel, seed, budget_s, cores)
     return {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(), "machine": os.uname().machine,
             "sample": f"{n} random output rows (b,t,h,w,head) of the workload, fp64 oracle, {dt:.1f} s"}
+
+
+# configurations whose oracle is also timed on one thread
+SINGLE_THREAD_CONFIGS = ("na3d_b1_t4_h8_w16_nh2_hd32_k3x5x5", "na3d_b1_t16_h64_w5_nh8_hd64_k3x5x5",
+                         "na3d_b2_t8_h64_w33_nh8_hd64_k3x7x33")
+
+
+def cpu_per_config(seed, budget_s=1.5):
+    """The fp64 oracle's useful GFLOP/s for every benchmark configuration, on
+    all host cores (and on one thread for the small ones). A row's work
+    depends only on the head dim and the window, so each is timed on rows of
+    a grid cut to at most 2K + 8 per axis and two heads (same HD, window and
+    border mix), which keeps input generation short."""
+    cores = os.cpu_count() or 1
+    table = {}
+    for name, (shape, kernel) in WORKLOADS.items():
+        B, T, H, W, NH, HD = shape
+        small = (1, min(T, 2 * kernel[0] + 8), min(H, 2 * kernel[1] + 8), min(W, 2 * kernel[2] + 8),
+                 min(NH, 2), HD)
+        tf, n, dt = oracle_sample_rate(small, kernel, seed, budget_s, cores)
+        row = {"gflops_all_cores": tf * 1e3, "cores": cores, "rows": n, "grid": list(small)}
+        if name in SINGLE_THREAD_CONFIGS:
+            tf1, n1, _ = oracle_sample_rate(small, kernel, seed, budget_s, 1)
+            row["gflops_1_thread"] = tf1 * 1e3
+        table[name] = row
+    return table
 
 
 def run_reference(args):
