@@ -543,7 +543,19 @@ __device__ __forceinline__ float write_probabilities(const float* s, const uint3
     for (int q = 0; q < C::NW; ++q) {
         if (q * 32 < n_mma) {
             uint32_t pk[16];
-            if (live[q]) {
+            if (live[q] && __all_sync(0xffffffffu, m[q] == 0xffffffffu)) {
+                // every key of this word is in every row's window: no selects
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float e0, e1;
+                    f2_unpack(f2_fma(f2_pack(s[32 * q + 2 * j], s[32 * q + 2 * j + 1]), l2e2, neg2), e0, e1);
+                    e0 = ex2_approx(e0);
+                    e1 = ex2_approx(e1);
+                    pk[j] = pack_bf16x2(e0, e1);
+                    if (j & 1) acc1 = f2_add(acc1, f2_pack(e0, e1));
+                    else acc0 = f2_add(acc0, f2_pack(e0, e1));
+                }
+            } else if (live[q]) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const float x0 = ((m[q] >> (2 * j)) & 1u) ? s[32 * q + 2 * j] : -INFINITY;
