@@ -244,6 +244,40 @@ def test_axis_flip_equivariance(axis):
     np.testing.assert_allclose(out_f, np.flip(out, axis=axis), rtol=1e-12, atol=1e-13)
 
 
+# ---------------------------------------------------------------- P6 dimension reduction
+
+def test_one_frame_window_isolates_frames():
+    """KT = 1 is 2-D neighborhood attention in each frame: the 3-D result of
+    frame t equals the oracle on that frame alone (a grid with T = 1)."""
+    shape = (2, 4, 6, 7, 2, 16)
+    kernel = (1, 3, 5)
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=31)
+    out = oracle.na3d_fwd(q, k, v, kernel)
+    for t in range(shape[1]):
+        sl = [np.ascontiguousarray(x[:, t:t + 1]) for x in (q, k, v)]
+        np.testing.assert_allclose(out[:, t:t + 1], oracle.na3d_fwd(*sl, kernel), rtol=1e-13, atol=1e-14)
+
+
+def test_one_dimensional_grid_is_a_sliding_window_along_t():
+    """H = W = 1 is 1-D neighborhood attention along T: for each frame t the
+    K frames starting at clamp(t - K//2, 0, T - K), a softmax over their
+    scores and the weighted sum of their values, written out here with
+    numpy for each (batch, head, frame)."""
+    B, T, NH, HD, K = 2, 23, 3, 16, 5
+    q, k, v = na3d_inputs.make_qkv(B, T, 1, 1, NH, HD, seed=32)
+    got = oracle.na3d_fwd(q, k, v, (K, 1, 1))
+    qd, kd, vd = f64(q)[:, :, 0, 0], f64(k)[:, :, 0, 0], f64(v)[:, :, 0, 0]
+    want = np.empty_like(qd)
+    for b in range(B):
+        for n in range(NH):
+            for t in range(T):
+                s0 = min(max(t - K // 2, 0), T - K)
+                x = kd[b, s0:s0 + K, n] @ qd[b, t, n]
+                p = np.exp(x - x.max())
+                want[b, t, n] = (p / p.sum()) @ vd[b, s0:s0 + K, n]
+    np.testing.assert_allclose(got[:, :, 0, 0], want, rtol=1e-12, atol=1e-13)
+
+
 # ---------------------------------------------------------------- P7 isolation
 
 def test_batch_head_isolation():
