@@ -149,6 +149,7 @@ struct Cfg {
     static_assert(LAG <= RING, "a product barrier never runs a phase ahead of its waiter");
     static_assert(SMEM_ALLOC * CPS <= 232448 && SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(NCAP == 64 || NCAP == 128, "score tile width");
+    static_assert(SW >= 64 || STEP == 2, "pairs of score words are adjacent in tensor memory");
     static_assert(NS >= 2, "K/V rings need two stages");
     static_assert(!FAST || (CWP == 8 || CWP == 16 || CWP == 32), "fast-path chunk stride");
 };
@@ -785,23 +786,8 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
         ChunkCursor cur{U.lo_t, 0, 0};
 
         for (int c = 0; c < U.nch; ++c, ++g) {
-            if (!sy.wait(sy.bar(C::B_SFULL + g % C::RING), (g / C::RING) & 1u)) return;
-            tc_fence_after();
-            // this chunk's ring slot: S words 0.. start there (wrapping to the
-            // first slot after the last), and P goes over its first SW columns
-            const uint32_t slot = C::slot_of(g);
-            const uint32_t p_addr = t_row + C::TM_R + slot * C::SW;
-            float s[C::NCAP];   // loaded asynchronously; not read before tmem_wait_ld
-#pragma unroll
-            for (int q = 0; q < C::NW; ++q) {
-                if (q * 32 < p.n_mma) {
-                    uint32_t sl = slot + (32u * q) / C::SW;
-                    sl = sl >= static_cast<uint32_t>(C::NSLOT) ? sl - C::NSLOT : sl;
-                    tmem_ld32(t_row + C::TM_R + sl * C::SW + (32u * q) % C::SW, s + 32 * q);
-                }
-            }
-            // The window mask of this chunk is built while the score loads are in flight.
-            // chunk geometry for this row (independent of the scores)
+            // The window mask of this chunk depends only on its position: it is
+            // built before the wait for its scores, off the chain from S to P.
             const int kh0 = U.lo_h + cur.hc * p.cr, kw0 = U.lo_w + cur.wc * p.cw;
             const bool t_ok = valid && static_cast<unsigned>(cur.kt - sT) < static_cast<unsigned>(p.KT);
             uint32_t m[4] = {0u, 0u, 0u, 0u};   // generic path: per-key mask
@@ -835,6 +821,24 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
             bool has_keys;
             if constexpr (C::FAST) has_keys = rowbits != 0u;
             else has_keys = (m[0] | m[1] | m[2] | m[3]) != 0u;
+
+            if (!sy.wait(sy.bar(C::B_SFULL + g % C::RING), (g / C::RING) & 1u)) return;
+            tc_fence_after();
+            // this chunk's ring slot: S words 0.. start there (wrapping to the
+            // first slot after the last), and P goes over its first SW columns
+            const uint32_t slot = C::slot_of(g);
+            const uint32_t p_addr = t_row + C::TM_R + slot * C::SW;
+            float s[C::NCAP];   // loaded asynchronously; not read before tmem_wait_ld
+            // words 2k and 2k+1 are adjacent columns (in one slot, or in a
+            // pair of slots that never wraps): one load each
+#pragma unroll
+            for (int q = 0; q < C::NW; q += 2) {
+                if (q * 32 < p.n_mma) {
+                    uint32_t sl = slot + (32u * q) / C::SW;
+                    sl = sl >= static_cast<uint32_t>(C::NSLOT) ? sl - C::NSLOT : sl;
+                    tmem_ld64(t_row + C::TM_R + sl * C::SW + (32u * q) % C::SW, s + 32 * q);
+                }
+            }
 
             tmem_wait_ld();
             tc_fence_before();
