@@ -293,23 +293,45 @@ def run_ours(args):
     plan = na.na3d_plan(*shape[1:], *kernel)
     executed = plan["chunks_per_slice"] * shape[0] * shape[4] * 128 * plan["n_mma"] * shape[5] * 4.0
 
-    # e2e: pinned host -> HBM copies of q, k, v, the kernel, HBM -> pinned host copy of out
+    # e2e: every step copies its q, k, v from pinned host memory to HBM, runs the kernel and
+    # copies its output back to pinned host memory. Steps are pipelined as a serving loop runs
+    # them: two device buffer sets, the copy-in of step i+1 and the copy-out of step i-1 on
+    # their own streams while step i computes; a buffer set is refilled only after the step
+    # that used it has finished with it.
     e2e_steps = max(3, min(args.steps, 30))
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    bufs = [(q, k, v, out), tuple(torch.empty_like(q) for _ in range(4))]
+    host_outs = [host_out, torch.empty(shape, dtype=torch.bfloat16).pin_memory()]
+    done_compute, done_out = [None, None], [None, None]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier(pg)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(e2e_steps)]
-    with torch.cuda.stream(stream):
-        for a, b in ev:
-            a.record(stream)
-            for dst, src in zip((q, k, v), host):
+    start.record(s_in)
+    for i in range(e2e_steps):
+        j = i % 2
+        qb, kb, vb, ob = bufs[j]
+        with torch.cuda.stream(s_in):
+            if done_compute[j] is not None:
+                s_in.wait_event(done_compute[j])
+            for dst, src in zip((qb, kb, vb), host):
                 dst.copy_(src, non_blocking=True)
-            na.na3d_fwd(q, k, v, out, kernel, stream=stream)
-            host_out.copy_(out, non_blocking=True)
-            b.record(stream)
+            copied = torch.cuda.Event()
+            copied.record(s_in)
+        stream.wait_event(copied)
+        if done_out[j] is not None:
+            stream.wait_event(done_out[j])
+        na.na3d_fwd(qb, kb, vb, ob, kernel, stream=stream)
+        done_compute[j] = torch.cuda.Event()
+        done_compute[j].record(stream)
+        s_out.wait_event(done_compute[j])
+        with torch.cuda.stream(s_out):
+            host_outs[j].copy_(ob, non_blocking=True)
+            done_out[j] = torch.cuda.Event()
+            done_out[j].record(s_out)
+    end.record(s_out)   # after the last copy-out, which follows every earlier step's work
     torch.cuda.synchronize()
     barrier(pg)
-    e2e_s = allreduce_max(pg, sum(a.elapsed_time(b) for a, b in ev) * 1e-3) / e2e_steps
+    e2e_s = allreduce_max(pg, start.elapsed_time(end) * 1e-3) / e2e_steps
     _ = float(host_out.view(torch.int16)[0, 0, 0, 0, 0, 0].item())  # the read-back result
 
     result = {
@@ -355,6 +377,8 @@ def run_ours(args):
             "d2h_bytes_per_step": n * 2,
             "ms_per_step": e2e_s * 1e3,
             "steps": e2e_steps,
+            "mode": "steps pipelined over two device buffer sets: copy-in, kernel and copy-out "
+                    "on separate streams",
         },
         "gpu_launches": args.steps,
         "clocks": clk,
