@@ -145,32 +145,12 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(uint32_t M, uint32_t N, u
            | ((M >> 4) << 24);    // M / 16
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T: A is read from tensor memory (lane = row,
-// each 32-bit column holds two consecutive bf16 K elements).
-__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Same MMAs with the descriptors given as 32-bit halves (only the low half,
-// the start address, changes between k-steps) and a compile-time accumulate
-// flag, so one issue is a couple of integer adds and the MMA itself.
+// D[tmem] (+)= A * B^T, issued by one thread, with the smem descriptors given
+// as 32-bit halves (only the low half, the start address, changes between
+// k-steps) and a compile-time accumulate flag, so one issue is a couple of
+// integer adds and the MMA itself. The _ss form reads A from shared memory;
+// the _ts form reads A from tensor memory (lane = row, each 32-bit column
+// holds two consecutive bf16 K elements).
 template <uint32_t ACC>
 __device__ __forceinline__ void umma_ss_halves(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
                                                uint32_t b_lo, uint32_t b_hi, uint32_t idesc) {
@@ -350,12 +330,6 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return d;
 }
 
-__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
 // Move registers between warpgroups (all warps of the warpgroup execute it).
 template <uint32_t N>
 __device__ __forceinline__ void regs_increase() {
@@ -365,10 +339,6 @@ __device__ __forceinline__ void regs_increase() {
 template <uint32_t N>
 __device__ __forceinline__ void regs_decrease() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 }  // namespace na3d
