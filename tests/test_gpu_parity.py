@@ -206,6 +206,29 @@ def test_repeated_launches_are_bit_identical(shape, kernel):
             np.testing.assert_array_equal(got, first)
 
 
+def test_concurrent_launches_on_two_streams():
+    """Two launches in flight at once on different streams (an HD-64 and an
+    HD-128 problem, several units per CTA): their CTAs may share SMs and the
+    tensor memory of an SM. Each result equals its launch alone, bit for bit,
+    and the device reports no wait that ran out."""
+    cases = [((1, 8, 32, 48, 4, 64), (3, 7, 7), 41), ((1, 6, 24, 40, 4, 128), (3, 5, 7), 42)]
+    alone, dev = [], []
+    for shape, kernel, seed in cases:
+        q, k, v = na3d_inputs.make_qkv(*shape, seed=seed)
+        alone.append(run_gpu(q, k, v, kernel))
+        dev.append((to_dev(q), to_dev(k), to_dev(v), kernel))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for _ in range(3):
+        outs = [torch.full_like(d[0], float("nan")) for d in dev]
+        torch.cuda.synchronize()
+        for (qd, kd, vd, kernel), out, st in zip(dev, outs, streams):
+            na.na3d_fwd(qd, kd, vd, out, kernel, stream=st)
+        torch.cuda.synchronize()
+        assert na.na3d_device_status() == 0
+        for out, want in zip(outs, alone):
+            np.testing.assert_array_equal(from_dev(out), want)
+
+
 def test_invalid_device_arguments_are_rejected():
     shape = (1, 4, 8, 16, 2, 32)
     x = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
