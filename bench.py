@@ -131,7 +131,8 @@ def ncu_traffic(workload):
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "clocks.mem,clocks.max.mem")
     NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_id):
@@ -166,8 +167,15 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
-        for line in self.lines:
+        return self.summarize(self.lines)
+
+    @classmethod
+    def summarize(cls, lines):
+        """Median SM and memory clocks, maximum clocks, median power and the
+        throttle reasons seen active, from `nvidia-smi --query-gpu=FIELDS
+        --format=csv,noheader,nounits` lines."""
+        sm, smax, mem, mmax, power, reasons = [], [], [], [], [], set()
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -176,11 +184,19 @@ class ClockSampler:
                 smax.append(float(parts[2]))
             except ValueError:
                 continue
-            for name, val in zip(self.NAMES, parts[5:9]):
+            for name, val in zip(cls.NAMES, parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
+            for dst, i in ((power, 3), (mem, 9), (mmax, 10)):
+                try:
+                    dst.append(float(parts[i]))
+                except (ValueError, IndexError):
+                    pass
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
+                "mem_mhz": statistics.median(mem) if mem else None,
+                "mem_max_mhz": max(mmax) if mmax else None,
+                "power_w": statistics.median(power) if power else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
