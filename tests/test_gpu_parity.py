@@ -183,7 +183,8 @@ def test_deterministic_and_stream_independent():
 
 @pytest.mark.parametrize("shape,kernel", [((1, 16, 64, 64, 8, 64), (3, 7, 7)),
                                           ((1, 16, 64, 5, 8, 64), (3, 5, 5)),
-                                          ((2, 8, 48, 48, 8, 128), (3, 7, 7))],
+                                          ((2, 8, 48, 48, 8, 128), (3, 7, 7)),
+                                          ((1, 8, 32, 40, 8, 256), (3, 5, 7))],
                          ids=lambda x: "x".join(map(str, x)))
 def test_repeated_launches_are_bit_identical(shape, kernel):
     """Shapes with many work units per CTA: every per-chunk pipeline barrier

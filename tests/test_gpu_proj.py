@@ -71,6 +71,23 @@ def test_projection_matches_the_oracle(M, C, NH, HD, with_bias):
     check_projection(from_dev(qkv), x, w, b, NH, HD, f"proj M={M} C={C} NH={NH} HD={HD}")
 
 
+def test_full_size_projection_on_sampled_rows():
+    """The benchmark's projection (65536 tokens, C = 512, 8 heads of 64: the
+    headline attention's q, k, v) in its own launch configuration; rows are
+    independent, so the oracle checks a random sample of them plus the first
+    and last tile."""
+    M, C, NH, HD = 65536, 512, 8, 64
+    x, w, b = make(M, C, NH, HD, seed=5, with_bias=True)
+    qkv = torch.empty((M, 3 * NH * HD), dtype=torch.bfloat16, device="cuda")
+    na.na3d_qkv_proj(to_dev(x), to_dev(w), to_dev(b), qkv, NH, HD)
+    torch.cuda.synchronize()
+    assert na.na3d_device_status() == 0
+    got = from_dev(qkv)
+    rng = np.random.default_rng(6)
+    rows = np.unique(np.concatenate([np.arange(128), np.arange(M - 128, M), rng.integers(0, M, 768)]))
+    check_projection(got[rows], x[rows], w, b, NH, HD, f"proj M={M} sampled {rows.size} rows")
+
+
 def test_unaligned_output_uses_16_byte_stores():
     M, C, NH, HD = 513, 128, 2, 64
     x, w, b = make(M, C, NH, HD, seed=5, with_bias=True)
