@@ -88,9 +88,37 @@ def na3d_status_string(status: int) -> str:
     return load_library().na3d_status_string(int(status)).decode()
 
 
-def _stream_handle(stream) -> int:
-    if stream is None:
+_torch = None
+_cuda_ok = None   # torch.cuda.is_available(), fixed for the process
+
+
+def _torch_module():
+    global _torch, _cuda_ok
+    if _torch is None:
         import torch
+        _torch = torch
+        _cuda_ok = torch.cuda.is_available()
+    return _torch
+
+
+def _check_bf16_on_device(tensors):
+    """Each (name, tensor) is a bf16 tensor on the current CUDA device: the
+    kernels get raw pointers, so a host or other-device tensor must not pass."""
+    torch = _torch_module()
+    dev = torch.cuda.current_device() if _cuda_ok else -2
+    for name, t in tensors:
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype is not torch.bfloat16 or t.get_device() != dev:
+            raise TypeError(f"{name} must be a bfloat16 tensor on the current CUDA device")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:   # the current torch stream of the current device
+        torch = _torch_module()
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return raw(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
@@ -104,20 +132,16 @@ def na3d_fwd(q, k, v, out, kernel_size, stream=None) -> None:
     odd. ``out`` is written in place. Runs asynchronously on ``stream``
     (default: the current torch stream). Raises NA3DError on a bad argument.
     """
-    import torch
-    lib = load_library()
-    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
-        if not isinstance(t, torch.Tensor):
-            raise TypeError(f"{name} must be a torch.Tensor")
-        if t.dtype != torch.bfloat16 or not t.is_cuda:
-            raise TypeError(f"{name} must be a bfloat16 CUDA tensor")
-        if t.dim() != 6 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous 6-D (B,T,H,W,NH,HD) tensor")
-        if tuple(t.shape) != tuple(q.shape):
-            raise ValueError("q, k, v and out must have the same shape")
+    lib = _lib if _lib is not None else load_library()
+    _check_bf16_on_device((("q", q), ("k", k), ("v", v), ("out", out)))
+    shape = q.shape
+    if len(shape) != 6 or k.shape != shape or v.shape != shape or out.shape != shape:
+        raise ValueError("q, k, v and out must have the same 6-D (B,T,H,W,NH,HD) shape")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous() and out.is_contiguous()):
+        raise ValueError("q, k, v and out must be contiguous")
     KT, KH, KW = (int(x) for x in kernel_size)
     rc = lib.na3d_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                      *[int(x) for x in q.shape], KT, KH, KW, _stream_handle(stream))
+                      *shape, KT, KH, KW, _stream_handle(stream))
     if rc != NA3D_OK:
         raise NA3DError(rc, "na3d_fwd")
 
@@ -139,13 +163,9 @@ def na3d_fwd_strided(q, k, v, out, kernel_size, stream=None) -> None:
     slices ``x[..., 0, :, :]``, ``x[..., 1, :, :]``, ``x[..., 2, :, :]`` of a
     fused projection output ``x`` of shape (B, T, H, W, 3, NH, HD). ``out`` is
     a contiguous (B, T, H, W, NH, HD) bf16 CUDA tensor."""
-    import torch
     lib = load_library()
-    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
-        if not isinstance(t, torch.Tensor):
-            raise TypeError(f"{name} must be a torch.Tensor")
-        if t.dtype != torch.bfloat16 or not t.is_cuda:
-            raise TypeError(f"{name} must be a bfloat16 CUDA tensor")
+    _check_bf16_on_device((("q", q), ("k", k), ("v", v), ("out", out)))
+    for t in (q, k, v, out):
         if t.dim() != 6 or tuple(t.shape) != tuple(q.shape):
             raise ValueError("q, k, v and out must have the same 6-D shape")
     if not out.is_contiguous():
@@ -165,13 +185,9 @@ def na3d_fwd_region(q, k, v, out, kernel_size, offset, stream=None) -> None:
     (B, Tq, Hq, Wq, NH, HD), k and v (B, T, H, W, NH, HD). Every query keeps
     its window in the whole grid (global coordinates). q, k, v may be views
     with a token stride as in ``na3d_fwd_strided``; ``out`` is contiguous."""
-    import torch
     lib = load_library()
+    _check_bf16_on_device((("q", q), ("k", k), ("v", v), ("out", out)))
     for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
-        if not isinstance(t, torch.Tensor):
-            raise TypeError(f"{name} must be a torch.Tensor")
-        if t.dtype != torch.bfloat16 or not t.is_cuda:
-            raise TypeError(f"{name} must be a bfloat16 CUDA tensor")
         if t.dim() != 6:
             raise ValueError(f"{name} must be a 6-D tensor")
     if tuple(k.shape) != tuple(v.shape) or tuple(out.shape) != tuple(q.shape):
@@ -198,13 +214,11 @@ def na3d_qkv_proj(x, w, bias, qkv, num_heads, head_dim, stream=None) -> None:
     (..., C); w: (3*NH*HD, C); bias: (3*NH*HD,) or None; qkv: contiguous bf16
     with x's leading dimensions and 3*NH*HD elements per token, e.g.
     (B, T, H, W, 3, NH, HD). ``qkv_views`` gives the attention inputs."""
-    import torch
     lib = load_library()
     tensors = [("x", x), ("w", w), ("qkv", qkv)] + ([("bias", bias)] if bias is not None else [])
+    _check_bf16_on_device(tensors)
     for name, t in tensors:
-        if not isinstance(t, torch.Tensor):
-            raise TypeError(f"{name} must be a torch.Tensor")
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        if not t.is_contiguous():
             raise TypeError(f"{name} must be a contiguous bfloat16 CUDA tensor")
     NH, HD = int(num_heads), int(head_dim)
     C = int(x.shape[-1])
