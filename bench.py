@@ -580,6 +580,48 @@ def cpu_per_config(seed, budget_s=1.5):
     return table
 
 
+# The pages' own kernel benchmark shapes ("[Triton/Gluon] Add 3D neighborhood
+# flash attention (na3d_flash)", review thread, Performance table): B = 1,
+# HD = 64, with the gfx950 (MI350X) times of the Triton kernel, which include
+# a staging copy of v. The pages leave NH open (4, 8 or 32); NH = 8 here.
+PAGES_SHAPES = [
+    ((1, 18, 32, 48, 8, 64), (3, 7, 7), 1249.0),
+    ((1, 36, 64, 96, 8, 64), (3, 5, 5), 1910.0),
+    ((1, 40, 96, 96, 8, 64), (3, 5, 5), 3319.0),
+    ((1, 16, 80, 32, 8, 64), (11, 11, 11), 1153.0),
+    ((1, 79, 192, 192, 8, 64), (11, 11, 11), 99143.0),
+    ((1, 4, 8, 128, 8, 64), (3, 5, 27), 40.0),
+]
+
+
+def run_pages_shapes(args):
+    """Times the kernel on the pages' benchmark shapes (context: another
+    vendor's GPU and an unstated NH), L2 flushed between steps."""
+    import torch
+    import neighborhood_attention_video_gb300 as na
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    peaks, _ = load_peaks()
+    flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4 + 1024,
+                        dtype=torch.float32, device=dev)
+    rows = []
+    gen = torch.Generator(device=dev)
+    for shape, kernel, gfx950_us in PAGES_SHAPES:
+        gen.manual_seed(args.seed)
+        q = (torch.randn(shape, generator=gen, device=dev) * shape[-1] ** -0.5).to(torch.bfloat16)
+        k = torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16)
+        v = torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        t = statistics.median(time_kernel(shape, kernel, q, k, v, out, 20, 3, flush, stream))
+        terms = roofline_terms(shape, kernel, t, peaks)
+        rows.append({"shape_BTHWNH_HD": list(shape), "kernel": list(kernel), "us": t * 1e6,
+                     "useful_tflops": terms["useful_tflops"], "roofline_frac": terms["roofline_frac"],
+                     "pages_gfx950_us": gfx950_us})
+        del q, k, v, out
+    print(json.dumps({"pages_shapes": rows, "note": "NH = 8 assumed; the pages' times are for "
+                      "AMD MI350X and include a staging copy of v"}), flush=True)
+
+
 def run_reference(args):
     """The reference arm: the CPU oracle as it stands, on the host cores."""
     world, rank, local, pg = dist_setup(args)
@@ -639,10 +681,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-configs", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pages-shapes", action="store_true",
+                    help="time the pages' own benchmark shapes (context) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.pages_shapes:
+        run_pages_shapes(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
