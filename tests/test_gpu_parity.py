@@ -72,6 +72,8 @@ FULL_CASES = [
     ((1, 3, 5, 7, 2, 64), (3, 5, 7)),        # window = whole grid: full attention
     ((1, 16, 64, 64, 8, 64), (3, 7, 7)),     # benchmark shape, (3,7,7)
     ((1, 16, 64, 96, 8, 64), (3, 5, 5)),     # benchmark shape, (3,5,5)
+    ((1, 3, 6, 10, 64, 16), (3, 3, 5)),      # 64 heads of 16
+    ((64, 2, 3, 5, 2, 32), (1, 3, 5)),       # 64 small batches: many units over tiny grids
     ((1, 4, 8, 128, 8, 64), (3, 5, 27)),     # the pages' wide-KW benchmark shape (NH 8)
     ((1, 16, 80, 32, 8, 64), (11, 11, 11)),  # the pages' small (11,11,11) benchmark shape (NH 8)
 ]
