@@ -20,8 +20,9 @@
  *
  * The library allocates no memory and is safe to call from several host
  * threads at once. Its only state is a mutex-guarded cache of tiling plans
- * (keyed by grid and window sizes) and one device word that records a
- * pipeline-wait timeout (see na3d_device_status).
+ * (keyed by grid and window sizes) and, per device, one word that records a
+ * pipeline-wait timeout plus the small table of words through which
+ * na3d_device_status takes it (see there).
  */
 #ifndef NA3D_H
 #define NA3D_H
@@ -36,7 +37,7 @@ extern "C" {
 enum na3d_status {
     NA3D_OK = 0,
     NA3D_ERR_NULL = 1,           /* a required pointer is NULL */
-    NA3D_ERR_SHAPE = 2,          /* T, H, W or HD < 1, or B, NH < 0 */
+    NA3D_ERR_SHAPE = 2,          /* a size < 1, or a query box outside the grid */
     NA3D_ERR_KERNEL = 3,         /* a window length is even, < 1, or larger than its axis */
     NA3D_ERR_HEAD_DIM = 4,       /* HD is not a power of two >= 16 */
     NA3D_ERR_ALIGN = 5,          /* a tensor pointer is not 16-byte aligned */
@@ -51,16 +52,22 @@ enum na3d_status {
 /*
  * na3d_fwd - out = NA3D(q, k, v) for one bf16 (B,T,H,W,NH,HD) problem.
  *
+ * The operation of "[Triton/Gluon] Add 3D neighborhood flash attention
+ * (na3d_flash)" (ROCm/aiter pull request 5230), Technical Details: the query
+ * at (t,h,w) attends to the KT x KH x KW keys of its window, shifted inward at
+ * the grid borders so that it always holds KT*KH*KW keys (the start rule is
+ * stated at the top of this file); the launcher's convention that q arrives
+ * already multiplied by head_dim^-0.5 and that inputs and output share the
+ * (B,T,H,W,NH,HD) bf16 layout.
+ *
  * q, k, v, out: DEVICE pointers to contiguous row-major bf16 tensors of shape
  *   (B, T, H, W, NH, HD) (HD fastest), each 16-byte aligned. The caller owns
  *   all four buffers; the library neither allocates nor frees memory.
  *   q must already be scaled by HD^-0.5: no scale is applied. q, k and v are
  *   read only and may alias one another; out must not overlap any of them.
- * B: batch size, >= 0.  T, H, W: grid sizes, >= 1.  NH: heads, >= 0.
- *   B == 0 or NH == 0 is an empty problem: the call returns NA3D_OK after
- *   validating the sizes, enqueues nothing, and does not look at the
- *   pointers (which may be NULL).
- * HD: head dimension, a power of two in [16, 256].
+ * B: batch size, T, H, W: grid sizes, NH: heads, all >= 1 (a size < 1,
+ *   including an empty batch, returns NA3D_ERR_SHAPE).
+ * HD: head dimension, a power of two >= 16 (above 256: NA3D_ERR_UNSUPPORTED).
  * KT, KH, KW: odd window lengths with 1 <= KT <= T, 1 <= KH <= H, 1 <= KW <= W.
  * stream: a cudaStream_t on the current device (NULL = legacy default stream).
  *
@@ -151,8 +158,8 @@ int na3d_fwd_region(const void* q, const void* k, const void* v, void* out,
  * qkv: DEVICE pointer, bf16 (M, 3*NH*HD) row-major; must not overlap x, w or
  *   bias. x, w and qkv are 16-byte aligned; C is a multiple of 8 (16-byte
  *   rows), else NA3D_ERR_ALIGN.
- * M >= 0 tokens, NH >= 0 heads (either 0: nothing to do, pointers not
- *   looked at), C >= 1, HD a power of two >= 16.
+ * M >= 1 tokens, NH >= 1 heads, C >= 1 (else NA3D_ERR_SHAPE), HD a power
+ *   of two >= 16.
  * Asynchronous on `stream`; errors as for na3d_fwd. na3d_device_status also
  * reports a pipeline wait of this kernel that gave up.
  */
@@ -209,12 +216,18 @@ int na3d_plan(int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD,
               int64_t KT, int64_t KH, int64_t KW, na3d_plan_info* info);
 
 /*
- * na3d_device_status - synchronizes `stream` and reports whether any na3d
- * kernel on the current device gave up on a pipeline wait (a deadlock guard:
- * each wait inside the kernel is bounded, and a wait that runs out records a
- * flag, drains its in-flight copies, frees its tensor memory and returns).
- * Returns NA3D_ERR_DEVICE_TIMEOUT and clears the flag if it was set,
- * NA3D_ERR_CUDA if synchronization fails, else NA3D_OK.
+ * na3d_device_status - after the work already enqueued on `stream`, takes
+ * the current device's timeout flag and synchronizes `stream`. The flag is
+ * set by any na3d kernel on the device whose pipeline wait gave up (a
+ * deadlock guard: each wait inside the kernels is bounded, and a wait that
+ * runs out records the flag, drains its in-flight copies and MMAs, frees its
+ * tensor memory and returns, leaving part of its output unwritten).
+ * "Takes" means read and cleared in one atomic step on the device: each
+ * timeout is reported by exactly one call. The flag is per device, not per
+ * launch: with several threads or streams launching on one device, the call
+ * reports a timeout of any of their launches that completed before it.
+ * Returns NA3D_ERR_DEVICE_TIMEOUT if the flag was set, NA3D_ERR_CUDA if the
+ * enqueue or the synchronization fails, else NA3D_OK.
  */
 int na3d_device_status(void* stream);
 

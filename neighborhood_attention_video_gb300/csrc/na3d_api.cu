@@ -26,7 +26,7 @@ bool mul_ok(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a
 
 int validate_shape(int64_t B, int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t KT,
                    int64_t KH, int64_t KW) {
-    if (B < 0 || NH < 0 || T < 1 || H < 1 || W < 1 || HD < 1) return NA3D_ERR_SHAPE;
+    if (B < 1 || NH < 1 || T < 1 || H < 1 || W < 1 || HD < 1) return NA3D_ERR_SHAPE;
     const int64_t ks[3] = {KT, KH, KW}, ns[3] = {T, H, W};
     for (int a = 0; a < 3; ++a)
         if (ks[a] < 1 || (ks[a] & 1) == 0 || ks[a] > ns[a]) return NA3D_ERR_KERNEL;
@@ -34,7 +34,7 @@ int validate_shape(int64_t B, int64_t T, int64_t H, int64_t W, int64_t NH, int64
     // element count and byte size of one tensor must fit int64; TMA limits:
     // every global dimension < 2^32, every stride < 2^40 bytes.
     int64_t n = 1;
-    const int64_t dims[6] = {B > 0 ? B : 1, T, H, W, NH > 0 ? NH : 1, HD};
+    const int64_t dims[6] = {B, T, H, W, NH, HD};
     for (int i = 0; i < 6; ++i)
         if (!mul_ok(n, dims[i], &n)) return NA3D_ERR_OVERFLOW;
     if (!mul_ok(n, 2, &n)) return NA3D_ERR_OVERFLOW;
@@ -231,7 +231,7 @@ const char* na3d_status_string(int status) {
     switch (status) {
         case NA3D_OK: return "NA3D_OK";
         case NA3D_ERR_NULL: return "NA3D_ERR_NULL: a required pointer is NULL";
-        case NA3D_ERR_SHAPE: return "NA3D_ERR_SHAPE: T, H, W, HD must be >= 1 and B, NH >= 0";
+        case NA3D_ERR_SHAPE: return "NA3D_ERR_SHAPE: every size must be >= 1 (and a query box inside the grid)";
         case NA3D_ERR_KERNEL: return "NA3D_ERR_KERNEL: window lengths must be odd and within 1..axis length";
         case NA3D_ERR_HEAD_DIM: return "NA3D_ERR_HEAD_DIM: head dimension must be a power of two >= 16";
         case NA3D_ERR_ALIGN: return "NA3D_ERR_ALIGN: tensor pointers must be 16-byte aligned";
@@ -281,7 +281,6 @@ int fwd_region(const void* q, const void* k, const void* v, void* out, int64_t B
         return NA3D_ERR_SHAPE;
     const int64_t kv_tokens = B * T * H * W, q_tokens = B * Tq * Hq * Wq;
     const int64_t out_bytes = q_tokens * NH * HD * 2;
-    if (out_bytes == 0) return NA3D_OK;  // B == 0 or NH == 0: nothing to read or write
     if (!q || !k || !v || !out) return NA3D_ERR_NULL;
     const int64_t strides[3] = {q_token_stride, k_token_stride, v_token_stride};
     const int64_t tokens[3] = {q_tokens, kv_tokens, kv_tokens};
@@ -407,7 +406,7 @@ int na3d_fwd(const void* q, const void* k, const void* v, void* out, int64_t B, 
 
 int na3d_qkv_proj(const void* x, const void* w, const void* bias, void* qkv, int64_t M, int64_t C,
                   int64_t NH, int64_t HD, void* stream) {
-    if (M < 0 || NH < 0 || C < 1 || HD < 1) return NA3D_ERR_SHAPE;
+    if (M < 1 || NH < 1 || C < 1 || HD < 1) return NA3D_ERR_SHAPE;
     if (!is_pow2(HD) || HD < 16) return NA3D_ERR_HEAD_DIM;
     if (C % 8 != 0) return NA3D_ERR_ALIGN;   // rows of x and W must be 16-byte aligned
     int64_t N, xb, wb, ob;
@@ -416,7 +415,6 @@ int na3d_qkv_proj(const void* x, const void* w, const void* bias, void* qkv, int
         return NA3D_ERR_OVERFLOW;
     if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || C >= (int64_t(1) << 31))
         return NA3D_ERR_OVERFLOW;
-    if (ob == 0) return NA3D_OK;   // no tokens or no heads: nothing to write
     if (!x || !w || !qkv) return NA3D_ERR_NULL;
     const void* ptrs[3] = {x, w, qkv};
     for (const void* p : ptrs)
@@ -458,8 +456,8 @@ int na3d_qkv_proj(const void* x, const void* w, const void* bias, void* qkv, int
 
 int na3d_device_status(void* stream) {
     unsigned int flag = 0, pflag = 0;
-    if (na3d::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &flag) != cudaSuccess ||
-        na3d::read_and_clear_proj_error(static_cast<cudaStream_t>(stream), &pflag) != cudaSuccess)
+    if (na3d::take_device_error(static_cast<cudaStream_t>(stream), &flag) != cudaSuccess ||
+        na3d::take_proj_error(static_cast<cudaStream_t>(stream), &pflag) != cudaSuccess)
         return NA3D_ERR_CUDA;
     return (flag || pflag) ? NA3D_ERR_DEVICE_TIMEOUT : NA3D_OK;
 }

@@ -45,6 +45,8 @@
 // the tensor memory is freed before the CTA exits.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "na3d_kernel.cuh"
 #include "sm103_ptx.cuh"
 
@@ -262,6 +264,12 @@ __device__ __forceinline__ bool wait_spin(uint32_t b, uint32_t parity, volatile 
         }
     }
 }
+// Wait for copies or MMAs in flight before the CTA frees its tensor memory
+// and exits; a drain that gives up is recorded like any other timeout.
+__device__ __forceinline__ void drain_wait(uint32_t b, uint32_t parity) {
+    if (!mbar_wait_bounded(b, parity, kDrainLimitNs)) atomicOr(&g_na3d_timeout_flag, 1u);
+}
+
 struct Sync {
     uint32_t bar0;                     // smem address of barrier 0
     volatile uint32_t* abort_flag;     // smem, shared by all roles
@@ -343,13 +351,13 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tq, cons
     // Drain: every issued load must land before the CTA may exit.
     for (uint32_t s = 0; s < C::NS; ++s) {
         const uint32_t fk = gk / C::NS + (s < gk % C::NS ? 1u : 0u);
-        if (fk) mbar_wait_bounded(sy.bar(C::B_KFULL + s), (fk - 1u) & 1u, kDrainLimitNs);
+        if (fk) drain_wait(sy.bar(C::B_KFULL + s), (fk - 1u) & 1u);
         const uint32_t fv = gv / C::NS + (s < gv % C::NS ? 1u : 0u);
-        if (fv) mbar_wait_bounded(sy.bar(C::B_VFULL + s), (fv - 1u) & 1u, kDrainLimitNs);
+        if (fv) drain_wait(sy.bar(C::B_VFULL + s), (fv - 1u) & 1u);
     }
     for (uint32_t s = 0; s < C::NQ; ++s) {
         const uint32_t fq = nq / C::NQ + (s < nq % C::NQ ? 1u : 0u);
-        if (fq) mbar_wait_bounded(sy.bar(C::B_QFULL + s), (fq - 1u) & 1u, kDrainLimitNs);
+        if (fq) drain_wait(sy.bar(C::B_QFULL + s), (fq - 1u) & 1u);
     }
 }
 
@@ -492,7 +500,7 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
     }
     // Drain: all MMAs issued by this thread complete before TMEM is freed.
     umma_commit(sy.bar(C::B_DRAIN));
-    mbar_wait_bounded(sy.bar(C::B_DRAIN), 0, kDrainLimitNs);
+    drain_wait(sy.bar(C::B_DRAIN), 0);
 }
 
 // Products: O += P V with P read from tensor memory; the unit's first
@@ -526,7 +534,7 @@ __device__ void mma_pv_role(const KernelParams& p, const Sync& sy, uint32_t base
         w.next(p);
     }
     umma_commit(sy.bar(C::B_DRAIN2));
-    mbar_wait_bounded(sy.bar(C::B_DRAIN2), 0, kDrainLimitNs);
+    drain_wait(sy.bar(C::B_DRAIN2), 0);
 }
 
 // ------------------------------------------------------------------ softmax
@@ -683,6 +691,14 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
     const int M = p.bt * p.bh * p.bw;
     const int iw = r % p.bw, ih = (r / p.bw) % p.bh, it = r / (p.bw * p.bh);
     uint32_t g = 0, ul = 0;
+    // A wait whose outcome the whole warp shares (the .sync.aligned tensor
+    // memory instructions that follow need every lane); a warp that gives up
+    // first waits for its own tensor-memory stores, then leaves.
+    auto swait = [&](uint32_t b, uint32_t parity) -> bool {
+        const bool ok = __all_sync(0xffffffffu, sy.wait(b, parity));
+        if (!ok) tmem_wait_st();
+        return ok;
+    };
 
     // Qx row of the brick of unit X (local head-group index `v`): -2^40 where
     // this row's query does not see the chunk column, 0 elsewhere; published
@@ -690,7 +706,7 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
     auto publish_qx = [&](uint32_t v, const Unit& X) -> bool {
         if constexpr (C::FAST) {
             const uint32_t xb = v % C::NQX;
-            if (!sy.wait(sy.bar(C::B_XEMPTY + xb), ((v / C::NQX) & 1u) ^ 1u)) return false;
+            if (!swait(sy.bar(C::B_XEMPTY + xb), ((v / C::NQX) & 1u) ^ 1u)) return false;
             const int t = X.t0 + it, h = X.h0 + ih, w = X.w0 + iw;
             const bool ok = r < M && t < p.Tq && h < p.Hq && w < p.Wq;
             const int c_lo = win_start(p.w_off + w, p.KW, p.W) - X.lo_w;
@@ -751,7 +767,7 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
             }
         }
         if (e_live) {   // the previous unit's epilogue: O / l -> bf16 -> global
-            if (!sy.wait(sy.bar(C::B_OFULL), e_ul & 1u)) return;
+            if (!swait(sy.bar(C::B_OFULL), e_ul & 1u)) return;
             tc_fence_after();
             const float inv = (e_valid && e_l > 0.f) ? rcp_approx(e_l) : 0.f;
 #pragma unroll 1
@@ -822,7 +838,7 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
             if constexpr (C::FAST) has_keys = rowbits != 0u;
             else has_keys = (m[0] | m[1] | m[2] | m[3]) != 0u;
 
-            if (!sy.wait(sy.bar(C::B_SFULL + g % C::RING), (g / C::RING) & 1u)) return;
+            if (!swait(sy.bar(C::B_SFULL + g % C::RING), (g / C::RING) & 1u)) return;
             tc_fence_after();
             // this chunk's ring slot: S words 0.. start there (wrapping to the
             // first slot after the last), and P goes over its first SW columns
@@ -901,7 +917,7 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
                 // O holds the products up to chunk g-1 (one of this unit: the
                 // reference maximum was finite); the last of them must be done
                 const uint32_t pc = g - 1u;
-                if (!sy.wait(sy.bar(C::B_PFREE + pc % C::RING), (pc / C::RING) & 1u)) return;
+                if (!swait(sy.bar(C::B_PFREE + pc % C::RING), (pc / C::RING) & 1u)) return;
                 tc_fence_after();
                 const float a = rescale ? alpha : 1.f;
 #pragma unroll 1
@@ -1081,16 +1097,26 @@ cudaError_t launch_fwd(int hd, int cwp, const CUtensorMap& tq, const CUtensorMap
     return cudaErrorInvalidValue;
 }
 
-cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* flag) {
-    cudaError_t e = cudaStreamSynchronize(stream);
+// Each status request takes the flag with one atomic exchange (so a timeout is
+// reported to exactly one request, never lost between a read and a clear) and
+// leaves the old value in a slot of its own, which the host then reads.
+constexpr unsigned int kStatusSlots = 256;
+__device__ unsigned int g_na3d_status_slots[kStatusSlots];
+
+__global__ void take_timeout_flag(unsigned int slot) {
+    g_na3d_status_slots[slot] = atomicExch(&g_na3d_timeout_flag, 0u);
+}
+
+cudaError_t take_device_error(cudaStream_t stream, unsigned int* flag) {
+    static std::atomic<unsigned int> next{0};
+    const unsigned int slot = next.fetch_add(1u) % kStatusSlots;
+    take_timeout_flag<<<1, 1, 0, stream>>>(slot);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = cudaMemcpyFromSymbol(flag, g_na3d_timeout_flag, sizeof(unsigned int));
+    e = cudaMemcpyFromSymbolAsync(flag, g_na3d_status_slots, sizeof(unsigned int),
+                                  slot * sizeof(unsigned int), cudaMemcpyDeviceToHost, stream);
     if (e != cudaSuccess) return e;
-    if (*flag) {
-        const unsigned int zero = 0;
-        e = cudaMemcpyToSymbol(g_na3d_timeout_flag, &zero, sizeof(unsigned int));
-    }
-    return e;
+    return cudaStreamSynchronize(stream);
 }
 
 }  // namespace na3d

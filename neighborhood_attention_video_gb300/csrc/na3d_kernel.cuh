@@ -63,7 +63,8 @@ cudaError_t launch_fwd(int hd, int cwp, const CUtensorMap& tq, const CUtensorMap
                        const CUtensorMap& tv, const KernelParams& kp, int grid,
                        cudaStream_t stream);
 
-// Read (and clear) the device-side timeout flag of the current device.
-cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* flag);
+// After the work already on `stream`, take (read and clear in one atomic
+// step) the timeout flag of the current device, then synchronize `stream`.
+cudaError_t take_device_error(cudaStream_t stream, unsigned int* flag);
 
 }  // namespace na3d

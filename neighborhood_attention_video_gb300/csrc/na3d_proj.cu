@@ -20,6 +20,7 @@
 // so a tile's epilogue overlaps the next tile's MMAs. Tiles run N-fastest:
 // CTAs working at the same time share the x tile through L2, and W stays in
 // L2. Every wait is bounded as in the attention kernel.
+#include <atomic>
 #include "na3d_proj.cuh"
 #include "sm103_ptx.cuh"
 
@@ -120,7 +121,8 @@ qkv_proj_sm103(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         // every issued load lands before the CTA may exit
         for (uint32_t s = 0; s < kStages; ++s) {
             const uint32_t f = it / kStages + (s < it % kStages ? 1u : 0u);
-            if (f) mbar_wait_bounded(sy.bar(B_FULL + s), (f - 1u) & 1u, kDrainLimitNs);
+            if (f && !mbar_wait_bounded(sy.bar(B_FULL + s), (f - 1u) & 1u, kDrainLimitNs))
+                atomicOr(&g_proj_timeout_flag, 1u);
         }
     } else if (warp == 5 && lane == 0) {
         // ---------------------------------------------------------- MMA issuer
@@ -154,7 +156,7 @@ qkv_proj_sm103(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             umma_commit(sy.bar(B_AFULL + buf));
         }
         umma_commit(sy.bar(B_DRAIN));
-        mbar_wait_bounded(sy.bar(B_DRAIN), 0, kDrainLimitNs);
+        if (!mbar_wait_bounded(sy.bar(B_DRAIN), 0, kDrainLimitNs)) atomicOr(&g_proj_timeout_flag, 1u);
     } else if (warp < 4) {
         // ---------------------------------------------------------- epilogue
         const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
@@ -236,16 +238,25 @@ cudaError_t launch_qkv_proj(const CUtensorMap& tx, const CUtensorMap& tw, const 
     return cudaGetLastError();
 }
 
-cudaError_t read_and_clear_proj_error(cudaStream_t stream, unsigned int* flag) {
-    cudaError_t e = cudaStreamSynchronize(stream);
+// The flag is taken as for the attention kernel: one atomic exchange per
+// status request, its old value left in a slot of that request's own.
+constexpr unsigned int kStatusSlots = 256;
+__device__ unsigned int g_proj_status_slots[kStatusSlots];
+
+__global__ void take_proj_flag(unsigned int slot) {
+    g_proj_status_slots[slot] = atomicExch(&g_proj_timeout_flag, 0u);
+}
+
+cudaError_t take_proj_error(cudaStream_t stream, unsigned int* flag) {
+    static std::atomic<unsigned int> next{0};
+    const unsigned int slot = next.fetch_add(1u) % kStatusSlots;
+    take_proj_flag<<<1, 1, 0, stream>>>(slot);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = cudaMemcpyFromSymbol(flag, g_proj_timeout_flag, sizeof(unsigned int));
+    e = cudaMemcpyFromSymbolAsync(flag, g_proj_status_slots, sizeof(unsigned int),
+                                  slot * sizeof(unsigned int), cudaMemcpyDeviceToHost, stream);
     if (e != cudaSuccess) return e;
-    if (*flag) {
-        const unsigned int zero = 0;
-        e = cudaMemcpyToSymbol(g_proj_timeout_flag, &zero, sizeof(unsigned int));
-    }
-    return e;
+    return cudaStreamSynchronize(stream);
 }
 
 }  // namespace na3d

@@ -25,7 +25,8 @@ struct ProjParams {
 cudaError_t launch_qkv_proj(const CUtensorMap& tx, const CUtensorMap& tw, const ProjParams& pp,
                             int grid, cudaStream_t stream);
 
-// Read (and clear) the projection kernel's device-side timeout flag.
-cudaError_t read_and_clear_proj_error(cudaStream_t stream, unsigned int* flag);
+// After the work already on `stream`, take (read and clear in one atomic
+// step) the projection kernel's timeout flag, then synchronize `stream`.
+cudaError_t take_proj_error(cudaStream_t stream, unsigned int* flag);
 
 }  // namespace na3d

@@ -25,16 +25,16 @@ def test_clock_summary_of_nothing():
 
 
 def test_roofline_terms_of_the_headline_workload():
-    """(1,16,64,64,8,64) with window (3,7,7): 4 * L * NH * HD * 147 useful
+    """(2,16,96,128,16,128) with window (3,7,7): 4 * L * NH * HD * 147 useful
     flops and four bf16 tensors of L * NH * HD elements."""
     shape, kernel = bench.WORKLOADS[bench.HEADLINE]
-    L = 16 * 64 * 64
-    flops = 4.0 * L * 8 * 64 * 147
-    nbytes = 4.0 * L * 8 * 64 * 2
+    L = 2 * 16 * 96 * 128
+    flops = 4.0 * L * 16 * 128 * 147
+    nbytes = 4.0 * L * 16 * 128 * 2
     assert bench.useful_flops(shape, kernel) == flops
     assert bench.min_bytes(shape) == nbytes
     peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1500.0}
-    t = 100e-6
+    t = 2000e-6
     r = bench.roofline_terms(shape, kernel, t, peaks)
     assert r["bound"] == "hbm"   # 147 / 2 flop per byte is below the ridge of 333
     assert abs(r["roofline_us"] - nbytes / 6000e9 * 1e6) < 1e-9

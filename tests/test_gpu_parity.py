@@ -252,10 +252,11 @@ def test_invalid_device_arguments_are_rejected():
     assert e.value.status == 5
 
 
-def test_empty_batch_is_a_no_op():
+def test_empty_batch_is_rejected():
     x = torch.zeros((0, 4, 8, 16, 2, 32), dtype=torch.bfloat16, device="cuda")
-    na.na3d_fwd(x, x, x, torch.empty_like(x), (3, 5, 5))
-    torch.cuda.synchronize()
+    with pytest.raises(na.NA3DError) as e:
+        na.na3d_fwd(x, x, x, torch.empty_like(x), (3, 5, 5))
+    assert e.value.status == 2
 
 
 @pytest.mark.parametrize("hd", [64, 128])

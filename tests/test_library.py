@@ -126,8 +126,8 @@ def test_region_validation(lib):
         assert call_region(lib, ptrs, box) == ERR_SHAPE, box
     # the window is checked against the grid, not the box
     assert call_region(lib, ptrs, (0, 0, 0, T, H, 3), kernel=(3, 5, 17)) == ERR_KERNEL
-    # empty batch: nothing to do, pointers not looked at
-    assert call_region(lib, (0, 0, 0, 0), (0, 0, 4, T, H, 4), dims=(0, T, H, W, 2, 32)) == OK
+    # an empty batch is a size below 1
+    assert call_region(lib, ptrs, (0, 0, 4, T, H, 4), dims=(0, T, H, W, 2, 32)) == ERR_SHAPE
     # out overlapping k, which spans the whole grid
     n_kv = 1 * T * H * W * 2 * 32 * 2
     assert call_region(lib, (base, base + (1 << 22), base + (2 << 22), base + (1 << 22) + n_kv // 2),
@@ -146,17 +146,22 @@ def test_qkv_proj_validation(lib):
     assert call(x, w, None, qkv, 1000, 60, 2, 32) == ERR_ALIGN    # rows of 120 bytes
     assert call(x, w, None, qkv, 1000, 64, 2, 48) == ERR_HEAD_DIM
     assert call(x, w, None, qkv, -1, 64, 2, 32) == ERR_SHAPE
-    assert call(0, 0, None, 0, 0, 64, 2, 32) == OK                  # no tokens: nothing to do
+    assert call(x, w, None, qkv, 0, 64, 2, 32) == ERR_SHAPE          # no tokens
+    assert call(x, w, None, qkv, 10, 64, 0, 32) == ERR_SHAPE         # no heads
     assert call(0, w, None, qkv, 10, 64, 2, 32) == ERR_NULL
     assert call(x + 8, w, None, qkv, 10, 64, 2, 32) == ERR_ALIGN
     assert call(x, w, None, x + 64, 10, 64, 2, 32) == ERR_ALIAS   # qkv over x
     assert call(x, w, qkv + 64, qkv, 10, 64, 2, 32) == ERR_ALIAS  # bias inside qkv
 
 
-def test_empty_problem_is_a_no_op(lib):
-    assert call_fwd(lib, (16, 32, 48, 64), dims=(0, 4, 8, 16, 2, 32)) == OK
-    assert call_fwd(lib, (16, 32, 48, 64), dims=(1, 4, 8, 16, 0, 32)) == OK
-    assert call_fwd(lib, (0, 0, 0, 0), dims=(0, 4, 8, 16, 2, 32)) == OK  # empty tensors may be NULL
+def test_empty_problem_is_rejected(lib):
+    """Every size must be at least 1: an empty batch or no heads is a shape
+    error, returned before the pointers are looked at."""
+    assert call_fwd(lib, (16, 32, 48, 64), dims=(0, 4, 8, 16, 2, 32)) == ERR_SHAPE
+    assert call_fwd(lib, (16, 32, 48, 64), dims=(1, 4, 8, 16, 0, 32)) == ERR_SHAPE
+    assert call_fwd(lib, (0, 0, 0, 0), dims=(0, 4, 8, 16, 2, 32)) == ERR_SHAPE
+    info = na.PlanInfo()
+    assert lib.na3d_plan(4, 8, 16, 0, 32, 3, 5, 5, ctypes.byref(info)) == ERR_SHAPE
 
 
 def test_valid_call_without_gpu_fails_loudly(lib):
