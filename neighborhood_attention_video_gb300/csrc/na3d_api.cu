@@ -38,11 +38,11 @@ int validate_shape(int64_t B, int64_t T, int64_t H, int64_t W, int64_t NH, int64
     for (int i = 0; i < 6; ++i)
         if (!mul_ok(n, dims[i], &n)) return NA3D_ERR_OVERFLOW;
     if (!mul_ok(n, 2, &n)) return NA3D_ERR_OVERFLOW;
-    if (NH * HD >= (int64_t(1) << 32) || W >= (int64_t(1) << 31) || H >= (int64_t(1) << 31) ||
+    // a head's column offset is a signed 32-bit TMA coordinate
+    if (NH * HD >= (int64_t(1) << 31) || W >= (int64_t(1) << 31) || H >= (int64_t(1) << 31) ||
         T >= (int64_t(1) << 31) || B >= (int64_t(1) << 31))
         return NA3D_ERR_OVERFLOW;
     if (n / dims[0] >= (int64_t(1) << 40)) return NA3D_ERR_OVERFLOW;  // batch stride in bytes
-    if (HD > 256) return NA3D_ERR_UNSUPPORTED;
     return NA3D_OK;
 }
 
@@ -240,7 +240,7 @@ const char* na3d_status_string(int status) {
         case NA3D_ERR_ARCH: return "NA3D_ERR_ARCH: the current device is not sm_103 (GB300)";
         case NA3D_ERR_CUDA: return "NA3D_ERR_CUDA: a CUDA call failed";
         case NA3D_ERR_DEVICE_TIMEOUT: return "NA3D_ERR_DEVICE_TIMEOUT: a pipeline wait in the kernel gave up";
-        case NA3D_ERR_UNSUPPORTED: return "NA3D_ERR_UNSUPPORTED: head dimension above 256 is not implemented";
+        case NA3D_ERR_UNSUPPORTED: return "NA3D_ERR_UNSUPPORTED: valid arguments this library does not implement";
         default: return "unknown na3d status";
     }
 }
@@ -324,14 +324,23 @@ int fwd_region(const void* q, const void* k, const void* v, void* out, int64_t B
     kp.nbh = int32_t((Hq + pl.bh - 1) / pl.bh);
     kp.nbw = int32_t((Wq + pl.bw - 1) / pl.bw);
     kp.cw = pl.cw; kp.cr = pl.cr; kp.n_mma = pl.n_mma;
-    const int64_t units = B * int64_t(kp.nbt) * kp.nbh * kp.nbw * NH;
+    // HD > 256: every head is cut into passes over 256 output columns, and a
+    // work unit is one (head, pass) pair of a brick
+    const int64_t npass = HD > 256 ? HD / 256 : 1;
+    int npass_log2 = 0;
+    while ((int64_t(1) << npass_log2) < npass) ++npass_log2;
+    const int64_t nv = NH * npass;   // (head, pass) pairs per token
+    kp.hd = int32_t(HD);
+    kp.nreg = int32_t(HD > 256 ? HD / 64 : 0);
+    kp.npass_log2 = npass_log2;
+    const int64_t units = B * int64_t(kp.nbt) * kp.nbh * kp.nbw * nv;
     if (units >= (int64_t(1) << 31)) return NA3D_ERR_OVERFLOW;
     kp.n_units = int32_t(units);
     kp.out = static_cast<uint16_t*>(out);
     // rows are HD * 2 >= 32 bytes: 32-byte stores when the base allows them
     kp.out_v8 = (reinterpret_cast<uintptr_t>(out) % 32u) == 0u ? 1 : 0;
     kp.withhold_k = withhold_k;
-    kp.div_nh = na3d::make_fastdiv(kp.NH);
+    kp.div_nh = na3d::make_fastdiv(int32_t(nv));
     kp.div_nbw = na3d::make_fastdiv(kp.nbw);
     kp.div_nbh = na3d::make_fastdiv(kp.nbh);
     kp.div_nbt = na3d::make_fastdiv(kp.nbt);
@@ -347,11 +356,11 @@ int fwd_region(const void* q, const void* k, const void* v, void* out, int64_t B
         return double(groups) / double(waves * slots);
     };
     double best = 0;
-    for (int64_t d = 1; d <= NH; d *= 2)
-        if (NH % d == 0 && balance(d) > best) best = balance(d);
+    for (int64_t d = 1; d <= nv; d *= 2)
+        if (nv % d == 0 && balance(d) > best) best = balance(d);
     kp.hg = 1;
-    for (int64_t d = 1; HD >= 128 && d <= NH; d *= 2)   // the kernel groups heads for HD >= 128
-        if (NH % d == 0 && balance(d) >= best - 0.03) kp.hg = int32_t(d);
+    for (int64_t d = 1; HD >= 128 && d <= nv; d *= 2)   // the kernel groups heads for HD >= 128
+        if (nv % d == 0 && balance(d) >= best - 0.03) kp.hg = int32_t(d);
 
     // Q over the query box, K and V over the whole grid
     CUtensorMap tq, tk, tv;

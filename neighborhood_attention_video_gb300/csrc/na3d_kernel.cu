@@ -75,6 +75,16 @@ struct Cfg {
     // applied by the tensor core (extra contraction block Qx Kx^T); CWP == 0:
     // per-element window masks in the softmax (any chunk geometry).
     static constexpr bool FAST = CWP > 0;
+    // WIDE (HD > 256): O of a whole row does not fit in tensor memory next to
+    // the score tiles. A work unit then computes one block of OB output
+    // columns (a "pass"; the head's NPASS passes are consecutive units), and
+    // the score contraction streams Q and K through one ring, one 64-column
+    // region of each per stage, instead of keeping the Q brick resident. Every
+    // pass recomputes the same scores (same MMA sequence, same probabilities).
+    // The one WIDE instance (HD = 512) serves every HD >= 512: the head size,
+    // its region count and its pass count come from the kernel parameters.
+    static constexpr bool WIDE = HD > 256;
+    static constexpr int OB = WIDE ? 256 : HD;      // output columns of a unit
     static constexpr int KEXT = FAST ? (CWP < 16 ? 16 : CWP) : 0;   // extra contraction columns
     static constexpr int XROWB = KEXT * 2;
     static constexpr uint32_t XSWZ = KEXT == 32 ? kSwizzle64B : kSwizzle32B;
@@ -83,18 +93,23 @@ struct Cfg {
     static constexpr int KX_TILE = NCAP * XROWB;
     static constexpr int RPW = FAST ? 32 / CWP : 0;  // chunk rows per 32-column word
     static constexpr int HDB = HD < 64 ? HD : 64;   // head-dim columns per TMA box / smem row
-    static constexpr int NREG = HD / HDB;           // boxes (smem regions) per tile
+    static constexpr int NREG = HD / HDB;           // boxes (smem regions) of a Q or K row (not WIDE)
+    static constexpr int VREG = OB / HDB;           // boxes of a V row block (= NREG unless WIDE)
     static constexpr int ROWB = HDB * 2;            // bytes per smem row
     static constexpr uint32_t SWZ = HDB == 64 ? kSwizzle128B : (HDB == 32 ? kSwizzle64B : kSwizzle32B);
     static constexpr int SBO = 8 * ROWB;            // stride between 8-row core groups
     static constexpr int Q_REG = 128 * ROWB;
-    static constexpr int Q_TILE = NREG * Q_REG;
+    static constexpr int Q_TILE = WIDE ? 0 : NREG * Q_REG;   // the resident Q brick
     static constexpr int KV_REG = NCAP * ROWB;
-    static constexpr int KV_TILE = NREG * KV_REG;
+    // one K stage: all regions of a chunk's K rows, or (WIDE) one region of the
+    // Q brick followed by the same region of the chunk's K rows
+    static constexpr int K_TILE = WIDE ? Q_REG + KV_REG : NREG * KV_REG;
+    static constexpr int V_TILE = VREG * KV_REG;
+    static constexpr int NSV = WIDE ? 2 : NS;       // V stages (K stages: NS)
     static constexpr int NW = NCAP / 32;            // 32-column words per score row
-    static constexpr int OPIECES = (HD + 31) / 32;  // 32-column TMEM loads per output row
+    static constexpr int OPIECES = (OB + 31) / 32;  // 32-column TMEM loads per output row
     static constexpr uint32_t TM_COLS = CPS == 2 ? 256 : 512;
-    static constexpr uint32_t TM_O = 0;                              // HD fp32 output columns
+    static constexpr uint32_t TM_O = 0;                              // OB fp32 output columns
     static constexpr uint32_t OCOLS = OPIECES * 32 < 64 ? 64 : OPIECES * 32;
     static constexpr uint32_t SW = NCAP / 2;                         // slot width = P columns
     static constexpr uint32_t TM_R = OCOLS;                          // first ring column
@@ -114,20 +129,20 @@ struct Cfg {
     static __device__ __forceinline__ uint32_t slot_of(uint32_t g) { return (g * STEP) % NSLOT; }
     // Shared memory: double-buffer Q and Qx where the per-SM share allows it.
     static constexpr int LIMIT = (CPS == 2 ? 115712 : 232448) - 1024 - 512;
-    static constexpr int FIXED = 2 * NS * KV_TILE + (FAST ? KX_TILE : 0);
-    static constexpr int NQ = FIXED + 2 * Q_TILE + (FAST ? 2 * QX_TILE : 0) <= LIMIT ? 2 : 1;
+    static constexpr int FIXED = NS * K_TILE + NSV * V_TILE + (FAST ? KX_TILE : 0);
+    static constexpr int NQ = WIDE ? 0 : (FIXED + 2 * Q_TILE + (FAST ? 2 * QX_TILE : 0) <= LIMIT ? 2 : 1);
     static constexpr int NQX = !FAST ? 0 : (FIXED + NQ * Q_TILE + 2 * QX_TILE <= LIMIT ? 2 : 1);
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
-    static constexpr int OFF_V = OFF_K + NS * KV_TILE;
-    static constexpr int OFF_QX = OFF_V + NS * KV_TILE;
+    static constexpr int OFF_V = OFF_K + NS * K_TILE;
+    static constexpr int OFF_QX = OFF_V + NSV * V_TILE;
     static constexpr int OFF_KX = OFF_QX + NQX * QX_TILE;
     static constexpr int OFF_BAR = OFF_KX + (FAST ? KX_TILE : 0);
     // barrier indices
     static constexpr int B_QFULL = 0, B_QEMPTY = NQ;
     static constexpr int B_KFULL = 2 * NQ, B_KEMPTY = B_KFULL + NS;
-    static constexpr int B_VFULL = B_KEMPTY + NS, B_VEMPTY = B_VFULL + NS;
-    static constexpr int B_XFULL = B_VEMPTY + NS, B_XEMPTY = B_XFULL + NQX;
+    static constexpr int B_VFULL = B_KEMPTY + NS, B_VEMPTY = B_VFULL + NSV;
+    static constexpr int B_XFULL = B_VEMPTY + NSV, B_XEMPTY = B_XFULL + NQX;
     // For chunk c: S(c) ready, S(c) read, P(c) written and the product of c
     // done are signalled on B_SFULL, B_SEMPTY, B_PFULL and B_PFREE + c % RING:
     // one barrier per ring position, so a softmax warp that runs ahead of the
@@ -152,8 +167,9 @@ struct Cfg {
     static_assert(SMEM_ALLOC * CPS <= 232448 && SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(NCAP == 64 || NCAP == 128, "score tile width");
     static_assert(SW >= 64 || STEP == 2, "pairs of score words are adjacent in tensor memory");
-    static_assert(NS >= 2, "K/V rings need two stages");
+    static_assert(NS >= 2 && NSV >= 2, "K/V rings need two stages");
     static_assert(!FAST || (CWP == 8 || CWP == 16 || CWP == 32), "fast-path chunk stride");
+    static_assert(!WIDE || (CPS == 1 && HDB == 64 && OB == 256 && STEP == 2), "wide instances");
 };
 
 // ------------------------------------------------------------------ geometry
@@ -291,73 +307,112 @@ struct ChunkCoords {
 template <class C>
 __device__ void producer_role(const KernelParams& p, const CUtensorMap* tq, const CUtensorMap* tk,
                               const CUtensorMap* tv, const Sync& sy, uint32_t base) {
-    uint32_t gk = 0, gv = 0, nq = 0;   // K chunks, V chunks and Q bricks issued
+    // K stages, V stages, chunks and Q bricks issued (WIDE: a K stage is one
+    // region of Q and K, so gk counts regions)
+    uint32_t gk = 0, gv = 0, gc = 0, nq = 0;
     ChunkCoords prev{0, 0, 0, 0, 0};
-    const uint32_t kv_bytes = C::NREG * C::ROWB * p.cw * p.cr;
+    // bytes of one K stage, one V stage and one Q brick (WIDE: of one region
+    // of the Q brick and of the K rows, which share a stage)
+    const uint32_t k_bytes = (C::WIDE ? 1 : C::NREG) * C::ROWB * p.cw * p.cr;
+    const uint32_t v_bytes = C::VREG * C::ROWB * p.cw * p.cr;
+    const uint32_t q_bytes = (C::WIDE ? 1 : C::NREG) * C::ROWB * p.bt * p.bh * p.bw;
 
     auto load_v = [&](const ChunkCoords& cc) -> bool {
-        const uint32_t st = gv % C::NS;
-        if (!sy.wait(sy.bar(C::B_VEMPTY + st), ((gv / C::NS) & 1u) ^ 1u)) return false;
+        const uint32_t st = gv % C::NSV;
+        if (!sy.wait(sy.bar(C::B_VEMPTY + st), ((gv / C::NSV) & 1u) ^ 1u)) return false;
         const uint32_t full = sy.bar(C::B_VFULL + st);
-        mbar_arrive_expect_tx(full, kv_bytes);
+        mbar_arrive_expect_tx(full, v_bytes);
 #pragma unroll
-        for (int r = 0; r < C::NREG; ++r)
-            tma_load_5d(base + C::OFF_V + st * C::KV_TILE + r * C::KV_REG, tv, full,
+        for (int r = 0; r < C::VREG; ++r)
+            tma_load_5d(base + C::OFF_V + st * C::V_TILE + r * C::KV_REG, tv, full,
                         cc.x + r * C::HDB, cc.kw0, cc.kh0, cc.kt, cc.b);
         ++gv;
         return true;
+    };
+    // one K stage; self-test of the bounded waits: CTA 0 may withhold one,
+    // whose barrier then never completes
+    auto begin_k = [&](uint32_t* full_out) -> int {
+        const uint32_t st = gk % C::NS;
+        if (!sy.wait(sy.bar(C::B_KEMPTY + st), ((gk / C::NS) & 1u) ^ 1u)) return -1;
+        *full_out = sy.bar(C::B_KFULL + st);
+        const bool send = blockIdx.x != 0 || static_cast<int>(gk) != p.withhold_k;
+        ++gk;
+        return send ? static_cast<int>(st) : -2;
     };
 
     bool ok = true;
     uint32_t ul = 0;
     for (int u = first_unit<C>(p); ok && u < p.n_units; u = next_unit<C>(p, u), ++ul) {
         const Unit U = unit_of(p, u);
-        const int xq = U.n * C::HD;
+        // U.n counts (head, pass) pairs when WIDE; the head's columns start at xq
+        const int head = C::WIDE ? U.n >> p.npass_log2 : U.n;
+        const int xq = head * (C::WIDE ? p.hd : C::HD);
+        const int xv = C::WIDE ? xq + (U.n & ((1 << p.npass_log2) - 1)) * C::OB : xq;
         ChunkCursor cur{U.lo_t, 0, 0};
         for (int c = 0; c < U.nch; ++c) {
-            const ChunkCoords cc{xq, U.lo_w + cur.wc * p.cw, U.lo_h + cur.hc * p.cr, cur.kt, U.b};
+            const ChunkCoords cc{xv, U.lo_w + cur.wc * p.cw, U.lo_h + cur.hc * p.cr, cur.kt, U.b};
             cur.advance(U);
-            const uint32_t st = gk % C::NS;
-            if (!sy.wait(sy.bar(C::B_KEMPTY + st), ((gk / C::NS) & 1u) ^ 1u)) { ok = false; break; }
-            const uint32_t full = sy.bar(C::B_KFULL + st);
-            // self-test of the bounded waits: CTA 0 may withhold one K chunk,
-            // whose barrier then never completes
-            if (blockIdx.x != 0 || static_cast<int>(gk) != p.withhold_k) {
-                mbar_arrive_expect_tx(full, kv_bytes);
+            if constexpr (C::WIDE) {
+                // region r of the Q brick and of the chunk's K rows, per stage
+                for (int r = 0; r < p.nreg; ++r) {
+                    uint32_t full;
+                    const int st = begin_k(&full);
+                    if (st == -1) { ok = false; break; }
+                    if (st >= 0) {
+                        const uint32_t dst = base + C::OFF_K + st * C::K_TILE;
+                        mbar_arrive_expect_tx(full, q_bytes + k_bytes);
+                        tma_load_5d(dst, tq, full, xq + r * C::HDB, U.w0, U.h0, U.t0, U.b);
+                        tma_load_5d(dst + C::Q_REG, tk, full, xq + r * C::HDB, cc.kw0, cc.kh0, cc.kt, cc.b);
+                    }
+                }
+                if (!ok) break;
+            } else {
+                uint32_t full;
+                const int st = begin_k(&full);
+                if (st == -1) { ok = false; break; }
+                if (st >= 0) {
+                    mbar_arrive_expect_tx(full, k_bytes);
 #pragma unroll
-                for (int r = 0; r < C::NREG; ++r)
-                    tma_load_5d(base + C::OFF_K + st * C::KV_TILE + r * C::KV_REG, tk, full,
-                                cc.x + r * C::HDB, cc.kw0, cc.kh0, cc.kt, cc.b);
+                    for (int r = 0; r < C::NREG; ++r)
+                        tma_load_5d(base + C::OFF_K + st * C::K_TILE + r * C::KV_REG, tk, full,
+                                    xq + r * C::HDB, cc.kw0, cc.kh0, cc.kt, cc.b);
+                }
             }
-            ++gk;
+            ++gc;
             // V trails K by one chunk; it goes before the unit's Q brick, whose
             // buffer may still be read by the previous unit's last score tile
-            if (gk >= 2 && !load_v(prev)) { ok = false; break; }
+            if (gc >= 2 && !load_v(prev)) { ok = false; break; }
             prev = cc;
-            if (c == 0) {  // the Q brick goes right behind the unit's first K chunk
-                const uint32_t qb = ul % C::NQ;
-                if (!sy.wait(sy.bar(C::B_QEMPTY + qb), ((ul / C::NQ) & 1u) ^ 1u)) { ok = false; break; }
-                const uint32_t qf = sy.bar(C::B_QFULL + qb);
-                mbar_arrive_expect_tx(qf, C::NREG * C::ROWB * p.bt * p.bh * p.bw);
+            if constexpr (!C::WIDE) {
+                if (c == 0) {  // the Q brick goes right behind the unit's first K chunk
+                    const uint32_t qb = ul % C::NQ;
+                    if (!sy.wait(sy.bar(C::B_QEMPTY + qb), ((ul / C::NQ) & 1u) ^ 1u)) { ok = false; break; }
+                    const uint32_t qf = sy.bar(C::B_QFULL + qb);
+                    mbar_arrive_expect_tx(qf, q_bytes);
 #pragma unroll
-                for (int r = 0; r < C::NREG; ++r)
-                    tma_load_5d(base + C::OFF_Q + qb * C::Q_TILE + r * C::Q_REG, tq, qf,
-                                xq + r * C::HDB, U.w0, U.h0, U.t0, U.b);
-                ++nq;
+                    for (int r = 0; r < C::NREG; ++r)
+                        tma_load_5d(base + C::OFF_Q + qb * C::Q_TILE + r * C::Q_REG, tq, qf,
+                                    xq + r * C::HDB, U.w0, U.h0, U.t0, U.b);
+                    ++nq;
+                }
             }
         }
     }
-    if (ok && gk > gv) load_v(prev);
+    if (ok && gc > gv) load_v(prev);
     // Drain: every issued load must land before the CTA may exit.
     for (uint32_t s = 0; s < C::NS; ++s) {
         const uint32_t fk = gk / C::NS + (s < gk % C::NS ? 1u : 0u);
         if (fk) drain_wait(sy.bar(C::B_KFULL + s), (fk - 1u) & 1u);
-        const uint32_t fv = gv / C::NS + (s < gv % C::NS ? 1u : 0u);
+    }
+    for (uint32_t s = 0; s < C::NSV; ++s) {
+        const uint32_t fv = gv / C::NSV + (s < gv % C::NSV ? 1u : 0u);
         if (fv) drain_wait(sy.bar(C::B_VFULL + s), (fv - 1u) & 1u);
     }
-    for (uint32_t s = 0; s < C::NQ; ++s) {
-        const uint32_t fq = nq / C::NQ + (s < nq % C::NQ ? 1u : 0u);
-        if (fq) drain_wait(sy.bar(C::B_QFULL + s), (fq - 1u) & 1u);
+    if constexpr (C::NQ > 0) {
+        for (uint32_t s = 0; s < C::NQ; ++s) {
+            const uint32_t fq = nq / C::NQ + (s < nq % C::NQ ? 1u : 0u);
+            if (fq) drain_wait(sy.bar(C::B_QFULL + s), (fq - 1u) & 1u);
+        }
     }
 }
 
@@ -440,7 +495,53 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
     };
     ChunkWalk<C> w;
     w.start(p);
-    while (w.more(p)) {
+    if constexpr (C::WIDE) {
+        // S(g) = sum over the NREG regions r of Q_r K_r^T, each region pair one
+        // stage of the K ring; never wraps (pairs of slots)
+        uint32_t gk = 0;   // K stages consumed
+        while (w.more(p)) {
+            uint32_t xb = 0;
+            if constexpr (C::FAST) {
+                xb = w.gl % C::NQX;
+                if (w.c == 0 && w.gfirst && !sy.wait(sy.bar(C::B_XFULL + xb), (w.gl / C::NQX) & 1u)) break;
+            }
+            if (w.g >= static_cast<uint32_t>(C::SLAG)) {
+                const uint32_t sc = w.g - C::SLAG;
+                if (!sy.wait(sy.bar(C::B_SEMPTY + sc % C::RING), (sc / C::RING) & 1u)) break;
+            }
+            if (w.g >= static_cast<uint32_t>(C::LAG)) {
+                const uint32_t pc = w.g - C::LAG;
+                if (!sy.wait(sy.bar(C::B_PFREE + pc % C::RING), (pc / C::RING) & 1u)) break;
+            }
+            const uint32_t d = tmem + C::TM_R + C::slot_of(w.g) * C::SW;
+            bool ok = true;
+            for (int r = 0; r < p.nreg; ++r, ++gk) {
+                const uint32_t st = gk % C::NS;
+                if (!sy.wait(sy.bar(C::B_KFULL + st), (gk / C::NS) & 1u)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t q_lo = static_cast<uint32_t>(kd0) + ((st * C::K_TILE) >> 4);
+                const uint32_t k_lo = q_lo + (C::Q_REG >> 4);
+                if (r == 0) umma_ss_halves<0>(d, q_lo, k_hi, k_lo, k_hi, idesc_s);
+                else umma_ss_halves<1>(d, q_lo, k_hi, k_lo, k_hi, idesc_s);
+#pragma unroll
+                for (int kk = 1; kk < C::HDB / 16; ++kk)
+                    umma_ss_halves<1>(d, q_lo + kk * 2, k_hi, k_lo + kk * 2, k_hi, idesc_s);
+                umma_commit(sy.bar(C::B_KEMPTY + st));
+            }
+            if (!ok) break;
+            if constexpr (C::FAST) {   // -2^40 on keys outside each row's W window
+                const uint32_t x_lo = x_lo0 + ((xb * C::QX_TILE) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < C::KEXT / 16; ++kk)
+                    umma_ss_halves<1>(d, x_lo + kk * 2, x_hi, y_lo + kk * 2, x_hi, idesc_s);
+            }
+            umma_commit(sy.bar(C::B_SFULL + w.g % C::RING));
+            if constexpr (C::FAST) {
+                if (w.c == w.nch - 1 && group_end<C>(p, w.u)) umma_commit(sy.bar(C::B_XEMPTY + xb));
+            }
+            w.next(p);
+        }
+    } else while (w.more(p)) {
         const uint32_t qb = w.ul % C::NQ, st = w.g % C::NS;
         if (w.c == 0 && !sy.wait(sy.bar(C::B_QFULL + qb), (w.ul / C::NQ) & 1u)) break;
         uint32_t xb = 0;
@@ -461,7 +562,7 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
         }
         tc_fence_after();
         const uint32_t q_lo = static_cast<uint32_t>(qd0) + ((qb * C::Q_TILE) >> 4);
-        const uint32_t k_lo = static_cast<uint32_t>(kd0) + ((st * C::KV_TILE) >> 4);
+        const uint32_t k_lo = static_cast<uint32_t>(kd0) + ((st * C::K_TILE) >> 4);
         const uint32_t x_lo = C::FAST ? x_lo0 + ((xb * C::QX_TILE) >> 4) : 0u;
         const uint32_t slot = C::slot_of(w.g);
         const uint32_t d = tmem + C::TM_R + slot * C::SW;
@@ -507,7 +608,7 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
 // product overwrites O, its last one signals the epilogue.
 template <class C>
 __device__ void mma_pv_role(const KernelParams& p, const Sync& sy, uint32_t base, uint32_t tmem) {
-    const uint32_t idesc_o = make_idesc_bf16(128, C::HD, 0, 1);
+    const uint32_t idesc_o = make_idesc_bf16(128, C::OB, 0, 1);
     const uint32_t d_o = tmem + C::TM_O;
     const uint64_t vd0 = make_smem_desc(base + C::OFF_V, C::KV_REG, C::SBO, C::SWZ);
     const uint32_t v_hi = static_cast<uint32_t>(vd0 >> 32);
@@ -515,12 +616,12 @@ __device__ void mma_pv_role(const KernelParams& p, const Sync& sy, uint32_t base
     ChunkWalk<C> w;
     w.start(p);
     while (w.more(p)) {
-        const uint32_t st = w.g % C::NS;
+        const uint32_t st = w.g % C::NSV;
         if (w.c == 0 && !sy.wait(sy.bar(C::B_OEMPTY), (w.ul & 1u) ^ 1u)) break;
-        if (!sy.wait(sy.bar(C::B_VFULL + st), (w.g / C::NS) & 1u)) break;
+        if (!sy.wait(sy.bar(C::B_VFULL + st), (w.g / C::NSV) & 1u)) break;
         if (!sy.wait(sy.bar(C::B_PFULL + w.g % C::RING), (w.g / C::RING) & 1u)) break;
         tc_fence_after();
-        const uint32_t v_lo = static_cast<uint32_t>(vd0) + ((st * C::KV_TILE) >> 4);
+        const uint32_t v_lo = static_cast<uint32_t>(vd0) + ((st * C::V_TILE) >> 4);
         const uint32_t a_p = tmem + C::TM_R + C::slot_of(w.g) * C::SW;
         if (w.c == 0) umma_ts_halves<0>(d_o, a_p, v_lo, v_hi, idesc_o);
         else umma_ts_halves<1>(d_o, a_p, v_lo, v_hi, idesc_o);
@@ -938,7 +1039,11 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
         // this unit's output is written at the top of the next iteration, once
         // the next unit is set up; its W masks go out now
         const int64_t tok = ((static_cast<int64_t>(U.b) * p.Tq + t) * p.Hq + h) * p.Wq + w;
-        e_orow = p.out + (tok * p.NH + U.n) * C::HD;
+        if constexpr (C::WIDE)   // U.n counts (head, pass) pairs; a pass writes OB columns
+            e_orow = p.out + (tok * p.NH + (U.n >> p.npass_log2)) * p.hd +
+                     (U.n & ((1 << p.npass_log2) - 1)) * C::OB;
+        else
+            e_orow = p.out + (tok * p.NH + U.n) * C::HD;
         e_l = l;
         e_ul = ul;
         e_valid = valid;
@@ -1072,11 +1177,13 @@ static void info_t(VariantInfo* v) {
     X(32, 128, 3, 2, CWP)     \
     X(64, 128, 2, 2, CWP)     \
     X(128, 64, 2, 2, CWP)     \
-    X(256, 64, 2, 1, CWP)
+    X(256, 64, 2, 1, CWP)     \
+    X(512, 64, 4, 1, CWP)
 #define NA3D_VARIANTS(X) \
     NA3D_HD_TABLE(X, 0) NA3D_HD_TABLE(X, 8) NA3D_HD_TABLE(X, 16) NA3D_HD_TABLE(X, 32)
 
 bool variant_info(int hd, int cwp, VariantInfo* info) {
+    if (hd > 256) hd = 512;   // the wide instance serves every HD >= 512
 #define X(hd_, n_, s_, c_, w_)                   \
     if (hd == hd_ && cwp == w_) {                \
         info_t<hd_, n_, s_, c_, w_>(info);       \
@@ -1090,6 +1197,7 @@ bool variant_info(int hd, int cwp, VariantInfo* info) {
 cudaError_t launch_fwd(int hd, int cwp, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const KernelParams& kp, int grid,
                        cudaStream_t stream) {
+    if (hd > 256) hd = 512;
 #define X(hd_, n_, s_, c_, w_) \
     if (hd == hd_ && cwp == w_) return launch_t<hd_, n_, s_, c_, w_>(tq, tk, tv, kp, grid, stream);
     NA3D_VARIANTS(X)

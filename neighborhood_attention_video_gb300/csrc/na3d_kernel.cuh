@@ -37,7 +37,11 @@ struct KernelParams {
     int32_t cw, cr, n_mma;   // chunk geometry and score-tile width
     int32_t n_units;         // B * nbt * nbh * nbw * NH (head fastest)
     int32_t hg;              // heads per group (a power of two dividing NH): a CTA runs the
-                             // hg heads of one brick back to back (1 for HD < 128)
+                             // hg heads of one brick back to back (1 for HD < 128); for
+                             // HD > 256 a "head" here is one (head, pass) pair
+    int32_t hd;              // head dimension (the instance's own unless HD > 256)
+    int32_t nreg;            // HD > 256: 64-column regions of a head (HD / 64)
+    int32_t npass_log2;      // HD > 256: log2 of the passes over 256 output columns
     uint16_t* out;           // bf16 output, (B,Tq,Hq,Wq,NH,HD)
     int32_t out_v8;          // 1: out is 32-byte aligned (32-byte stores), 0: 16-byte stores
     int32_t withhold_k;      // self-test: CTA 0 skips its K load number withhold_k (-1: none)
@@ -54,8 +58,9 @@ struct VariantInfo {
     int ctas_per_sm;  // resident CTAs per SM the instance is sized for
 };
 
-// Instances exist for HD in {16, 32, 64, 128, 256} and chunk stride cwp in
-// {0 (generic per-key masks), 8, 16, 32 (W window applied by the tensor core)}.
+// Instances exist for HD in {16, 32, 64, 128, 256, >= 512 (one instance for
+// every larger power of two)} and chunk stride cwp in {0 (generic per-key
+// masks), 8, 16, 32 (W window applied by the tensor core)}.
 bool variant_info(int hd, int cwp, VariantInfo* info);
 
 // Launch the instance for (hd, cwp) on `stream` with `grid` persistent CTAs.

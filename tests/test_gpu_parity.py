@@ -76,6 +76,10 @@ FULL_CASES = [
     ((64, 2, 3, 5, 2, 32), (1, 3, 5)),       # 64 small batches: many units over tiny grids
     ((1, 4, 8, 128, 8, 64), (3, 5, 27)),     # the pages' wide-KW benchmark shape (NH 8)
     ((1, 16, 80, 32, 8, 64), (11, 11, 11)),  # the pages' small (11,11,11) benchmark shape (NH 8)
+    ((1, 4, 9, 20, 2, 512), (3, 5, 7)),      # HD 512: two passes over 256 output columns
+    ((1, 3, 5, 40, 1, 512), (3, 3, 33)),     # HD 512 with per-key masks
+    ((2, 3, 6, 12, 3, 1024), (3, 3, 5)),     # HD 1024: four passes, B and NH > 1
+    ((1, 2, 4, 6, 1, 2048), (1, 3, 5)),      # HD 2048
 ]
 
 
@@ -154,7 +158,7 @@ def test_axis_flip_equivariance():
         assert rel < 5e-3, (axis, rel)
 
 
-@pytest.mark.parametrize("hd", [64, 128])
+@pytest.mark.parametrize("hd", [64, 128, 512])
 @pytest.mark.parametrize("kernel", [(3, 5, 7), (3, 7, 33)], ids=lambda x: "x".join(map(str, x)))
 def test_score_spike_in_a_later_chunk(kernel, hd):
     """Keys of the last frames are scaled up, so rows meet scores tens of log2
@@ -188,7 +192,8 @@ def test_deterministic_and_stream_independent():
 @pytest.mark.parametrize("shape,kernel", [((1, 16, 64, 64, 8, 64), (3, 7, 7)),
                                           ((1, 16, 64, 5, 8, 64), (3, 5, 5)),
                                           ((2, 8, 48, 48, 8, 128), (3, 7, 7)),
-                                          ((1, 8, 32, 40, 8, 256), (3, 5, 7))],
+                                          ((1, 8, 32, 40, 8, 256), (3, 5, 7)),
+                                          ((1, 6, 24, 40, 8, 512), (3, 5, 7))],
                          ids=lambda x: "x".join(map(str, x)))
 def test_repeated_launches_are_bit_identical(shape, kernel):
     """Shapes with many work units per CTA: every per-chunk pipeline barrier
@@ -259,7 +264,7 @@ def test_empty_batch_is_rejected():
     assert e.value.status == 2
 
 
-@pytest.mark.parametrize("hd", [64, 128])
+@pytest.mark.parametrize("hd", [64, 128, 512])
 @pytest.mark.parametrize("shift", [0, 8], ids=["out32B", "out16B"])
 def test_output_untouched_outside_the_tensor(shift, hd):
     """The kernel writes exactly the output tensor: guard bands around it keep
@@ -286,6 +291,7 @@ REGION_CASES = [
     ((1, 5, 9, 30, 2, 32), (3, 5, 11), (1, 2, 10, 2, 4, 4)),       # box narrower than the window
     ((1, 6, 10, 24, 2, 64), (5, 5, 5), (3, 5, 20, 3, 5, 4)),       # box at the far borders
     ((2, 5, 13, 19, 3, 128), (3, 5, 7), (1, 2, 3, 3, 8, 10)),      # HD 128, B and NH > 1
+    ((1, 5, 9, 21, 2, 512), (3, 5, 7), (1, 2, 6, 3, 5, 9)),        # HD 512
     ((1, 4, 9, 50, 2, 64), (3, 3, 33), (0, 0, 7, 4, 9, 30)),       # wide window: per-key masks
 ]
 
@@ -360,7 +366,8 @@ def test_region_with_strided_views():
 
 @pytest.mark.parametrize("shape,kernel", [((1, 6, 20, 36, 2, 64), (3, 7, 7)),
                                           ((2, 5, 13, 19, 3, 128), (3, 5, 7)),
-                                          ((1, 8, 24, 33, 2, 64), (3, 7, 33))],
+                                          ((1, 8, 24, 33, 2, 64), (3, 7, 33)),
+                                          ((1, 4, 9, 20, 2, 1024), (3, 5, 7))],
                          ids=lambda x: "x".join(map(str, x)))
 def test_fused_qkv_views_match_contiguous(shape, kernel):
     """q, k, v as the three slices of one fused [B,T,H,W,3,NH,HD] projection

@@ -64,7 +64,7 @@ def call_fwd(lib, ptrs=(16, 32, 48, 1 << 20), dims=(1, 4, 8, 16, 2, 32), kernel=
     ((1, 4, 8, 16, 2, 32), (3, 9, 5), ERR_KERNEL),      # KH > H
     ((1, 4, 8, 16, 2, 48), (3, 5, 5), ERR_HEAD_DIM),
     ((1, 4, 8, 16, 2, 8), (3, 5, 5), ERR_HEAD_DIM),
-    ((1, 4, 8, 16, 2, 512), (3, 5, 5), ERR_UNSUPPORTED),
+    ((1, 4, 8, 16, 1 << 22, 512), (3, 5, 5), ERR_OVERFLOW),   # NH * HD = 2^31 columns
     ((1 << 40, 4, 8, 16, 2, 32), (3, 5, 5), ERR_OVERFLOW),
 ])
 def test_shape_validation(lib, dims, kernel, code):
@@ -154,6 +154,13 @@ def test_qkv_proj_validation(lib):
     assert call(x, w, qkv + 64, qkv, 10, 64, 2, 32) == ERR_ALIAS  # bias inside qkv
 
 
+def test_every_power_of_two_head_dim_is_planned(lib):
+    """HD > 256 is served by one wide instance: 64-key tiles, 64-column boxes."""
+    for hd in (512, 1024, 2048, 4096):
+        p = na.na3d_plan(4, 8, 16, 2, hd, 3, 5, 5)
+        assert p["hd_box"] == 64 and p["n_mma"] <= 64
+
+
 def test_empty_problem_is_rejected(lib):
     """Every size must be at least 1: an empty batch or no heads is a shape
     error, returned before the pointers are looked at."""
@@ -234,6 +241,8 @@ def check_plan_covers_windows(T, H, W, HD, kernel):
     (16, 96, 128, 128, (3, 7, 7)),
     (8, 64, 33, 64, (3, 7, 33)),
     (5, 7, 200, 256, (3, 3, 161)),
+    (6, 9, 20, 512, (3, 5, 7)),
+    (3, 6, 40, 1024, (3, 3, 33)),
     (1, 1, 9, 16, (1, 1, 9)),
     (9, 1, 1, 16, (5, 1, 1)),
 ])
@@ -246,5 +255,5 @@ def test_plan_random_sweep(lib):
     for _ in range(40):
         T, H, W = (int(x) for x in rng.integers(1, 40, size=3))
         kernel = tuple(int(rng.choice(np.arange(1, n + 1, 2))) for n in (T, H, W))
-        HD = int(rng.choice([16, 32, 64, 128, 256]))
+        HD = int(rng.choice([16, 32, 64, 128, 256, 512, 2048]))
         check_plan_covers_windows(T, H, W, HD, kernel)
