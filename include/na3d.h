@@ -202,7 +202,10 @@ typedef struct na3d_plan_info {
     int64_t chunks_per_slice;     /* chunks per (batch, head) slice */
     int64_t smem_bytes;           /* dynamic shared memory per CTA */
     int32_t w_stride;             /* 8, 16 or 32: chunk rows padded to this many keys and the
-                                     W window applied by the tensor core; 0: per-key masks */
+                                     W window applied by the tensor core; 1: every W window
+                                     is the whole axis (KW == W), chunk rows are whole grid
+                                     rows and the H window is applied by the tensor core;
+                                     0: per-key masks */
     int32_t reserved;
 } na3d_plan_info;
 

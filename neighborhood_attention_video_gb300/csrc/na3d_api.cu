@@ -91,16 +91,26 @@ constexpr double kChunkOverhead = 24.0;
 constexpr double kBrickOverhead = 96.0;
 constexpr double kFastColumn = 0.55;
 
-Plan make_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap) {
+// Row-mask plans (every W window is the whole axis): the tensor core masks
+// the H window through halo-row columns, so a brick's halo may span at most
+// kRowsCols rows including chunk padding, in at most kRowsTiles h-chunks.
+constexpr int64_t kRowsCols = 15;
+constexpr int64_t kRowsTiles = 5;
+
+Plan make_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap, bool allow_rows) {
     const int64_t H = ah.n, W = aw.n, KH = ah.k, KW = aw.k;
     Plan best;
+    // mode 0: W windows by the tensor core (W unions up to 32 keys, a fixed
+    // power-of-two chunk stride) or per-key masks (wider unions);
+    // mode 1: whole-row W windows (KW == W), H windows by the tensor core
+    for (int mode = 0; mode < 2; ++mode) {
+    if (mode == 1 && !(allow_rows && KW == W && W <= ncap)) break;
     for (int64_t bw = 1; bw <= (aw.nq < 128 ? aw.nq : 128); ++bw) {
         const int64_t ew = (bw + KW - 1 < W) ? bw + KW - 1 : W;   // widest W union
-        // W unions of up to 32 keys use a fixed power-of-two chunk stride and
-        // the tensor-core W mask; wider ones the generic per-key masks.
         int64_t cwp = 0;
-        if (ew <= 32) cwp = ew <= 8 ? 8 : (ew <= 16 ? 16 : 32);
-        const int64_t cw = cwp ? cwp : (ew > ncap ? ncap : ew);
+        if (mode == 1) cwp = 1;
+        else if (ew <= 32) cwp = ew <= 8 ? 8 : (ew <= 16 ? 16 : 32);
+        const int64_t cw = cwp == 1 ? W : cwp ? cwp : (ew > ncap ? ncap : ew);
         const double col_cost = cwp ? kFastColumn : 1.0;
         int64_t nbw;
         const int64_t sw = axis_sum(aw, bw, cw, &nbw);
@@ -110,6 +120,10 @@ Plan make_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap) {
             if (cr_max > eh) cr_max = eh;
             // any row count up to the cap (fewer rows can mean fewer 32-key words)
             for (int64_t cr = cr_max; cr >= 1; --cr) {
+                if (cwp == 1) {   // the widest halo's rows must fit the mask columns
+                    const int64_t n_hc = (eh + cr - 1) / cr;
+                    if (n_hc > kRowsTiles || n_hc * cr > kRowsCols) continue;
+                }
                 const int64_t n_mma = (cr * cw + 15) / 16 * 16;
                 int64_t nbh;
                 const int64_t sh = axis_sum(ah, bh, cr, &nbh);
@@ -136,25 +150,26 @@ Plan make_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap) {
             }
         }
     }
+    }
     return best;
 }
 
 // Plans depend only on the grid, the query box, the window and the
 // score-tile cap; they are cached (bounded, mutex-guarded) because the search
 // takes ~0.1 ms.
-Plan cached_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap) {
+Plan cached_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap, bool allow_rows) {
     using Key = std::tuple<int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t,
-                           int64_t, int64_t, int64_t, int64_t, int>;
+                           int64_t, int64_t, int64_t, int64_t, int, bool>;
     static std::mutex mu;
     static std::map<Key, Plan> cache;
     const Key key{at.nq, at.off, at.n, at.k, ah.nq, ah.off, ah.n, ah.k,
-                  aw.nq, aw.off, aw.n, aw.k, ncap};
+                  aw.nq, aw.off, aw.n, aw.k, ncap, allow_rows};
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
-    Plan pl = make_plan(at, ah, aw, ncap);
+    Plan pl = make_plan(at, ah, aw, ncap, allow_rows);
     std::lock_guard<std::mutex> g(mu);
     if (cache.size() >= 1024) cache.clear();
     cache.emplace(key, pl);
@@ -252,7 +267,8 @@ int na3d_plan(int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t K
     if (rc != NA3D_OK) return rc;
     VariantInfo vi;
     if (!na3d::variant_info(int(HD), 0, &vi)) return NA3D_ERR_UNSUPPORTED;
-    const Plan pl = cached_plan(Axis{T, 0, T, KT}, Axis{H, 0, H, KH}, Axis{W, 0, W, KW}, vi.ncap);
+    const bool rows = na3d::variant_info(int(HD), 1, nullptr);
+    const Plan pl = cached_plan(Axis{T, 0, T, KT}, Axis{H, 0, H, KH}, Axis{W, 0, W, KW}, vi.ncap, rows);
     if (!na3d::variant_info(int(HD), pl.cwp, &vi)) return NA3D_ERR_UNSUPPORTED;
     info->bt = pl.bt; info->bh = pl.bh; info->bw = pl.bw;
     info->cw = pl.cw; info->cr = pl.cr; info->n_mma = pl.n_mma;
@@ -311,7 +327,8 @@ int fwd_region(const void* q, const void* k, const void* v, void* out, int64_t B
 
     VariantInfo vi;
     if (!na3d::variant_info(int(HD), 0, &vi)) return NA3D_ERR_UNSUPPORTED;
-    const Plan pl = cached_plan(Axis{Tq, t0, T, KT}, Axis{Hq, h0, H, KH}, Axis{Wq, w0, W, KW}, vi.ncap);
+    const bool rows = na3d::variant_info(int(HD), 1, nullptr);
+    const Plan pl = cached_plan(Axis{Tq, t0, T, KT}, Axis{Hq, h0, H, KH}, Axis{Wq, w0, W, KW}, vi.ncap, rows);
     if (!na3d::variant_info(int(HD), pl.cwp, &vi)) return NA3D_ERR_UNSUPPORTED;
 
     KernelParams kp;

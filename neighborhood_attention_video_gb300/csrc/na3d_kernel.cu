@@ -71,10 +71,20 @@ constexpr uint16_t kMaskBf16 = 0xD380u;
 template <int HD_, int NCAP_, int NS_, int CPS_, int CWP_>
 struct Cfg {
     static constexpr int HD = HD_, NCAP = NCAP_, NS = NS_, CPS = CPS_, CWP = CWP_;
-    // CWP > 0: chunk rows have a fixed stride of CWP keys and the W window is
+    // CWP > 1: chunk rows have a fixed stride of CWP keys and the W window is
     // applied by the tensor core (extra contraction block Qx Kx^T); CWP == 0:
     // per-element window masks in the softmax (any chunk geometry).
+    // CWP == 1 (ROWS): every W window is the whole axis (KW = W), chunk rows
+    // are whole grid rows, and the tensor core applies the H window instead:
+    // Kx marks each key's row within the brick's halo (one Kx tile per h-chunk
+    // index), Qx marks the halo rows outside each query's H window.
     static constexpr bool FAST = CWP > 0;
+    static constexpr bool ROWS = CWP == 1;
+    // softmax: columns per uniformly masked group (ROWS: 16, so that the
+    // validity bits end at the tile width, a multiple of 16)
+    static constexpr int RW = ROWS ? 16 : CWP;
+    static constexpr int NKX = ROWS ? 5 : 1;        // Kx tiles (ROWS: one per h-chunk index)
+    static constexpr int XDEAD = 15;                // ROWS: the Kx column of padding keys
     // WIDE (HD > 256): O of a whole row does not fit in tensor memory next to
     // the score tiles. A work unit then computes one block of OB output
     // columns (a "pass"; the head's NPASS passes are consecutive units), and
@@ -85,13 +95,13 @@ struct Cfg {
     // its region count and its pass count come from the kernel parameters.
     static constexpr bool WIDE = HD > 256;
     static constexpr int OB = WIDE ? 256 : HD;      // output columns of a unit
-    static constexpr int KEXT = FAST ? (CWP < 16 ? 16 : CWP) : 0;   // extra contraction columns
+    static constexpr int KEXT = FAST ? (CWP < 16 ? 16 : CWP) : 0;   // extra contraction columns (ROWS: 16)
     static constexpr int XROWB = KEXT * 2;
     static constexpr uint32_t XSWZ = KEXT == 32 ? kSwizzle64B : kSwizzle32B;
     static constexpr int XSBO = 8 * XROWB;
     static constexpr int QX_TILE = 128 * XROWB;
     static constexpr int KX_TILE = NCAP * XROWB;
-    static constexpr int RPW = FAST ? 32 / CWP : 0;  // chunk rows per 32-column word
+    static constexpr int RPW = FAST ? 32 / RW : 0;   // uniformly masked groups per 32-column word
     static constexpr int HDB = HD < 64 ? HD : 64;   // head-dim columns per TMA box / smem row
     static constexpr int NREG = HD / HDB;           // boxes (smem regions) of a Q or K row (not WIDE)
     static constexpr int VREG = OB / HDB;           // boxes of a V row block (= NREG unless WIDE)
@@ -129,7 +139,7 @@ struct Cfg {
     static __device__ __forceinline__ uint32_t slot_of(uint32_t g) { return (g * STEP) % NSLOT; }
     // Shared memory: double-buffer Q and Qx where the per-SM share allows it.
     static constexpr int LIMIT = (CPS == 2 ? 115712 : 232448) - 1024 - 512;
-    static constexpr int FIXED = NS * K_TILE + NSV * V_TILE + (FAST ? KX_TILE : 0);
+    static constexpr int FIXED = NS * K_TILE + NSV * V_TILE + (FAST ? NKX * KX_TILE : 0);
     static constexpr int NQ = WIDE ? 0 : (FIXED + 2 * Q_TILE + (FAST ? 2 * QX_TILE : 0) <= LIMIT ? 2 : 1);
     static constexpr int NQX = !FAST ? 0 : (FIXED + NQ * Q_TILE + 2 * QX_TILE <= LIMIT ? 2 : 1);
     static constexpr int OFF_Q = 0;
@@ -137,7 +147,7 @@ struct Cfg {
     static constexpr int OFF_V = OFF_K + NS * K_TILE;
     static constexpr int OFF_QX = OFF_V + NSV * V_TILE;
     static constexpr int OFF_KX = OFF_QX + NQX * QX_TILE;
-    static constexpr int OFF_BAR = OFF_KX + (FAST ? KX_TILE : 0);
+    static constexpr int OFF_BAR = OFF_KX + (FAST ? NKX * KX_TILE : 0);
     // barrier indices
     static constexpr int B_QFULL = 0, B_QEMPTY = NQ;
     static constexpr int B_KFULL = 2 * NQ, B_KEMPTY = B_KFULL + NS;
@@ -168,7 +178,8 @@ struct Cfg {
     static_assert(NCAP == 64 || NCAP == 128, "score tile width");
     static_assert(SW >= 64 || STEP == 2, "pairs of score words are adjacent in tensor memory");
     static_assert(NS >= 2 && NSV >= 2, "K/V rings need two stages");
-    static_assert(!FAST || (CWP == 8 || CWP == 16 || CWP == 32), "fast-path chunk stride");
+    static_assert(!FAST || (CWP == 1 || CWP == 8 || CWP == 16 || CWP == 32), "fast-path chunk stride");
+    static_assert(!ROWS || (KEXT == 16 && !WIDE), "row-mask instances");
     static_assert(!WIDE || (CPS == 1 && HDB == 64 && OB == 256 && STEP == 2), "wide instances");
 };
 
@@ -423,6 +434,7 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tq, cons
 template <class C>
 struct ChunkWalk {
     int u, c, nch;
+    int hc, n_hc;         // ROWS: h-chunk index of chunk c (one W segment per row)
     uint32_t ul, g, gl;   // local unit, global chunk and local head-group counters
     bool gfirst;          // the unit opens its head group
     __device__ __forceinline__ void start(const KernelParams& p) {
@@ -433,15 +445,27 @@ struct ChunkWalk {
         gl = 0;
         gfirst = true;
         nch = 0;
+        hc = 0;
+        n_hc = 1;
     }
     // false when the CTA has no units left; decodes a new unit's chunk count
     __device__ __forceinline__ bool more(const KernelParams& p) {
         if (u >= p.n_units) return false;
-        if (c == 0) nch = unit_of(p, u).nch;
+        if (c == 0) {
+            const Unit U = unit_of(p, u);
+            nch = U.nch;
+            if constexpr (C::ROWS) {
+                n_hc = U.n_hc;
+                hc = 0;
+            }
+        }
         return true;
     }
     __device__ __forceinline__ void next(const KernelParams& p) {
         ++g;
+        if constexpr (C::ROWS) {
+            if (++hc == n_hc) hc = 0;
+        }
         if (++c == nch) {
             c = 0;
             ++ul;
@@ -572,12 +596,14 @@ __device__ void mma_s_role(const KernelParams& p, const Sync& sy, uint32_t base,
         // per-key-mask instances measured faster with the halves written out.
         const bool wrap = C::STEP == 1 && slot + 1 == static_cast<uint32_t>(C::NSLOT);
         if constexpr (C::FAST) {
+            // ROWS: the Kx tile of this chunk's h-chunk index
+            const uint32_t y0 = C::ROWS ? y_lo + static_cast<uint32_t>(w.hc) * (C::KX_TILE >> 4) : y_lo;
             const int halves = wrap && n_hi > 0 ? 2 : 1;
 #pragma unroll 1
             for (int hh = 0; hh < halves; ++hh) {
                 const uint32_t dd = hh == 0 ? d : tmem + C::TM_R;
                 const uint32_t kl = hh == 0 ? k_lo : k_lo + ((C::SW * C::ROWB) >> 4);
-                const uint32_t yl = hh == 0 ? y_lo : y_lo + ((C::SW * C::XROWB) >> 4);
+                const uint32_t yl = hh == 0 ? y0 : y0 + ((C::SW * C::XROWB) >> 4);
                 const uint32_t id = !wrap ? idesc_s : (hh == 0 ? idesc_lo : idesc_hi);
                 issue(dd, q_lo, kl, x_lo, yl, id);
             }
@@ -735,8 +761,8 @@ __device__ __forceinline__ float fast_probabilities(const float* s, uint32_t row
                     const float nm = ((rowbits >> i) & 1u) ? -moff : -INFINITY;
                     const uint64_t nm2 = f2_pack(nm, nm);
 #pragma unroll
-                    for (int jj = 0; jj < C::CWP / 2; ++jj) {
-                        const int j = rr * (C::CWP / 2) + jj;
+                    for (int jj = 0; jj < C::RW / 2; ++jj) {
+                        const int j = rr * (C::RW / 2) + jj;
                         float e0, e1;
                         f2_unpack(f2_fma(f2_pack(s[32 * q + 2 * j], s[32 * q + 2 * j + 1]), l2e2, nm2),
                                   e0, e1);
@@ -773,8 +799,8 @@ __device__ __forceinline__ float fast_row_max(const float* s, uint32_t rowbits, 
                 const int i = q * C::RPW + rr;
                 float rm = -INFINITY;
 #pragma unroll
-                for (int jj = 0; jj < C::CWP; jj += 2) {
-                    const int b = 32 * q + rr * C::CWP + jj;
+                for (int jj = 0; jj < C::RW; jj += 2) {
+                    const int b = 32 * q + rr * C::RW + jj;
                     rm = max3f(rm, s[b], s[b + 1]);
                 }
                 mx = ((rowbits >> i) & 1u) ? fmaxf(mx, rm) : mx;
@@ -810,7 +836,12 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
             if (!swait(sy.bar(C::B_XEMPTY + xb), ((v / C::NQX) & 1u) ^ 1u)) return false;
             const int t = X.t0 + it, h = X.h0 + ih, w = X.w0 + iw;
             const bool ok = r < M && t < p.Tq && h < p.Hq && w < p.Wq;
-            const int c_lo = win_start(p.w_off + w, p.KW, p.W) - X.lo_w;
+            // column c masks W position c of a chunk row (the window starts at
+            // c_lo), or with ROWS halo row c (the H window starts at c_lo)
+            const int c_lo = C::ROWS ? win_start(p.h_off + h, p.KH, p.H) - X.lo_h
+                                     : win_start(p.w_off + w, p.KW, p.W) - X.lo_w;
+            const int klen = C::ROWS ? p.KH : p.KW;
+            const int ncol = C::ROWS ? C::XDEAD : C::CWP;   // columns that can be valid
             const uint32_t tile = base + C::OFF_QX + xb * C::QX_TILE;
 #pragma unroll
             for (int k = 0; k < C::XROWB / 16; ++k) {
@@ -818,8 +849,12 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int c0 = 8 * k + 2 * e, c1 = c0 + 1;
-                    const bool m0 = ok && c0 < C::CWP && static_cast<unsigned>(c0 - c_lo) >= static_cast<unsigned>(p.KW);
-                    const bool m1 = ok && c1 < C::CWP && static_cast<unsigned>(c1 - c_lo) >= static_cast<unsigned>(p.KW);
+                    bool m0 = ok && c0 < ncol && static_cast<unsigned>(c0 - c_lo) >= static_cast<unsigned>(klen);
+                    bool m1 = ok && c1 < ncol && static_cast<unsigned>(c1 - c_lo) >= static_cast<unsigned>(klen);
+                    if constexpr (C::ROWS) {   // padding keys are masked for every row
+                        m0 = m0 || c0 == C::XDEAD;
+                        m1 = m1 || c1 == C::XDEAD;
+                    }
                     wd[e] = (m0 ? kMaskBf16 : 0u) | ((m1 ? kMaskBf16 : 0u) << 16);
                 }
                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tile + swizzled_chunk(r, k, C::XROWB)),
@@ -911,7 +946,12 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
             uint32_t rowbits = 0u;              // fast path: valid chunk rows
             if (t_ok) {
                 const int i0 = max(sH - kh0, 0), i1 = min(sH + p.KH - kh0, p.cr);
-                if constexpr (C::FAST) {
+                if constexpr (C::ROWS) {
+                    // the tensor core masks single keys; a chunk with no row of
+                    // this query's H window is skipped as a whole; the groups
+                    // of 16 columns past the tile width hold no scores
+                    if (i0 < i1) rowbits = (1u << (p.n_mma >> 4)) - 1u;
+                } else if constexpr (C::FAST) {
                     if (i0 < i1) rowbits = ((1u << (i1 - i0)) - 1u) << i0;
                 } else {
                     const int c0 = max(sW - kw0, 0), c1 = min(sW + p.KW - kw0, p.cw);
@@ -1081,21 +1121,32 @@ na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int i = threadIdx.x; i < C::OFF_KX / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
     }
     if constexpr (C::FAST) {
-        // Kx: key j of a chunk has a one in column j % CWP (its W position).
+        // Kx: key j of a chunk has a one in column j % CWP (its W position);
+        // with ROWS, tile hc has it in the column of the key's row within the
+        // brick's halo (hc * cr + j / cw), or in the dead column for padding
+        // keys and rows past the last one a mask column can name.
         const int j = threadIdx.x;
         if (j < C::NCAP) {
-#pragma unroll
-            for (int k = 0; k < C::XROWB / 16; ++k) {
-                uint32_t wd[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c0 = 8 * k + 2 * e;
-                    wd[e] = (c0 == j % CWP ? 0x3F80u : 0u) | ((c0 + 1 == j % CWP ? 0x3F80u : 0u) << 16);
+#pragma unroll 1
+            for (int x = 0; x < C::NKX; ++x) {
+                int col = j % CWP;
+                if constexpr (C::ROWS) {
+                    col = j < p.cr * p.cw ? x * p.cr + j / p.cw : C::XDEAD;
+                    col = col < C::XDEAD ? col : C::XDEAD;
                 }
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                 base + C::OFF_KX + swizzled_chunk(j, k, C::XROWB)),
-                             "r"(wd[0]), "r"(wd[1]), "r"(wd[2]), "r"(wd[3])
-                             : "memory");
+#pragma unroll
+                for (int k = 0; k < C::XROWB / 16; ++k) {
+                    uint32_t wd[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c0 = 8 * k + 2 * e;
+                        wd[e] = (c0 == col ? 0x3F80u : 0u) | ((c0 + 1 == col ? 0x3F80u : 0u) << 16);
+                    }
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                     base + C::OFF_KX + x * C::KX_TILE + swizzled_chunk(j, k, C::XROWB)),
+                                 "r"(wd[0]), "r"(wd[1]), "r"(wd[2]), "r"(wd[3])
+                                 : "memory");
+                }
             }
         }
     }
@@ -1171,7 +1222,8 @@ static void info_t(VariantInfo* v) {
 }
 
 // The instance table: (HD, score-tile cap, K/V stages, CTAs per SM) x chunk
-// stride CWP (0: generic masks; 8, 16, 32: W window applied by the tensor core).
+// stride CWP (0: generic masks; 8, 16, 32: W window applied by the tensor core;
+// 1: whole-row W windows, H window applied by the tensor core).
 #define NA3D_HD_TABLE(X, CWP) \
     X(16, 128, 4, 2, CWP)     \
     X(32, 128, 3, 2, CWP)     \
@@ -1179,14 +1231,20 @@ static void info_t(VariantInfo* v) {
     X(128, 64, 2, 2, CWP)     \
     X(256, 64, 2, 1, CWP)     \
     X(512, 64, 4, 1, CWP)
+#define NA3D_ROWS_TABLE(X)  \
+    X(16, 128, 4, 2, 1)     \
+    X(32, 128, 3, 2, 1)     \
+    X(64, 128, 2, 2, 1)     \
+    X(128, 64, 2, 2, 1)     \
+    X(256, 64, 2, 1, 1)
 #define NA3D_VARIANTS(X) \
-    NA3D_HD_TABLE(X, 0) NA3D_HD_TABLE(X, 8) NA3D_HD_TABLE(X, 16) NA3D_HD_TABLE(X, 32)
+    NA3D_HD_TABLE(X, 0) NA3D_HD_TABLE(X, 8) NA3D_HD_TABLE(X, 16) NA3D_HD_TABLE(X, 32) NA3D_ROWS_TABLE(X)
 
 bool variant_info(int hd, int cwp, VariantInfo* info) {
     if (hd > 256) hd = 512;   // the wide instance serves every HD >= 512
 #define X(hd_, n_, s_, c_, w_)                   \
     if (hd == hd_ && cwp == w_) {                \
-        info_t<hd_, n_, s_, c_, w_>(info);       \
+        if (info) info_t<hd_, n_, s_, c_, w_>(info); \
         return true;                             \
     }
     NA3D_VARIANTS(X)

@@ -61,6 +61,7 @@ struct VariantInfo {
 // Instances exist for HD in {16, 32, 64, 128, 256, >= 512 (one instance for
 // every larger power of two)} and chunk stride cwp in {0 (generic per-key
 // masks), 8, 16, 32 (W window applied by the tensor core)}.
+// (info may be null: then only whether the instance exists)
 bool variant_info(int hd, int cwp, VariantInfo* info);
 
 // Launch the instance for (hd, cwp) on `stream` with `grid` persistent CTAs.

@@ -80,6 +80,13 @@ FULL_CASES = [
     ((1, 3, 5, 40, 1, 512), (3, 3, 33)),     # HD 512 with per-key masks
     ((2, 3, 6, 12, 3, 1024), (3, 3, 5)),     # HD 1024: four passes, B and NH > 1
     ((1, 2, 4, 6, 1, 2048), (1, 3, 5)),      # HD 2048
+    # whole-row W windows (KW = W): H windows applied by the tensor core
+    ((1, 4, 10, 21, 2, 128), (3, 5, 21)),    # HD 128
+    ((1, 5, 12, 9, 3, 32), (3, 3, 9)),       # HD 32
+    ((1, 3, 8, 13, 2, 256), (3, 5, 13)),     # HD 256 (one CTA per SM)
+    ((1, 4, 20, 3, 2, 16), (3, 7, 3)),       # HD 16, W = 3
+    ((2, 6, 30, 1, 2, 64), (3, 5, 1)),       # W = KW = 1
+    ((1, 7, 40, 17, 2, 64), (5, 11, 17)),    # tall H windows: many h-chunks per brick
 ]
 
 
@@ -175,6 +182,18 @@ def test_score_spike_in_a_later_chunk(kernel, hd):
     check(got, oracle.na3d_fwd(q, k, v, kernel), f"spike {shape} {kernel}")
 
 
+def test_score_spike_with_whole_row_windows():
+    """As above, with KW = W: the H window comes from the tensor core, and
+    the spiking rows must still raise the kept reference maximum."""
+    shape, kernel = (1, 6, 14, 33, 2, 64), (3, 7, 33)
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=31)
+    kf = na3d_inputs.bf16_bits_to_f64(k)
+    kf[:, 4:] *= 40.0
+    k = na3d_inputs.f64_to_bf16_bits(kf)
+    got = run_gpu(q, k, v, kernel)
+    check(got, oracle.na3d_fwd(q, k, v, kernel), f"spike {shape} {kernel}")
+
+
 # ------------------------------------------------------------ launch behaviour
 
 def test_deterministic_and_stream_independent():
@@ -193,7 +212,8 @@ def test_deterministic_and_stream_independent():
                                           ((1, 16, 64, 5, 8, 64), (3, 5, 5)),
                                           ((2, 8, 48, 48, 8, 128), (3, 7, 7)),
                                           ((1, 8, 32, 40, 8, 256), (3, 5, 7)),
-                                          ((1, 6, 24, 40, 8, 512), (3, 5, 7))],
+                                          ((1, 6, 24, 40, 8, 512), (3, 5, 7)),
+                                          ((2, 8, 64, 33, 8, 64), (3, 7, 33))],
                          ids=lambda x: "x".join(map(str, x)))
 def test_repeated_launches_are_bit_identical(shape, kernel):
     """Shapes with many work units per CTA: every per-chunk pipeline barrier
@@ -292,6 +312,8 @@ REGION_CASES = [
     ((1, 6, 10, 24, 2, 64), (5, 5, 5), (3, 5, 20, 3, 5, 4)),       # box at the far borders
     ((2, 5, 13, 19, 3, 128), (3, 5, 7), (1, 2, 3, 3, 8, 10)),      # HD 128, B and NH > 1
     ((1, 5, 9, 21, 2, 512), (3, 5, 7), (1, 2, 6, 3, 5, 9)),        # HD 512
+    ((1, 5, 14, 25, 2, 64), (3, 5, 25), (1, 3, 0, 3, 8, 25)),      # whole-row W windows
+    ((1, 5, 14, 25, 2, 64), (3, 5, 25), (0, 4, 5, 5, 7, 10)),      # whole-row W windows, W sub-box
     ((1, 4, 9, 50, 2, 64), (3, 3, 33), (0, 0, 7, 4, 9, 30)),       # wide window: per-key masks
 ]
 

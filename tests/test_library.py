@@ -217,6 +217,12 @@ def check_plan_covers_windows(T, H, W, HD, kernel):
                 hi = [starts[a][qs[a][-1]] + kernel[a] for a in range(3)]
                 n_hc = -(-(hi[1] - lo[1]) // cr)
                 n_wc = -(-(hi[2] - lo[2]) // cw)
+                if p["w_stride"] == 1:
+                    # whole-row W windows: one W segment, and the halo's rows
+                    # (chunk padding included) fit the 15 row-mask columns
+                    # and the 5 per-h-chunk mask tiles
+                    assert KW == W and cw == W and n_wc == 1
+                    assert n_hc * cr <= 15 and n_hc <= 5
                 total_chunks += (hi[0] - lo[0]) * n_hc * n_wc
                 cov_h = set()
                 for hc in range(n_hc):
@@ -243,6 +249,9 @@ def check_plan_covers_windows(T, H, W, HD, kernel):
     (5, 7, 200, 256, (3, 3, 161)),
     (6, 9, 20, 512, (3, 5, 7)),
     (3, 6, 40, 1024, (3, 3, 33)),
+    (7, 40, 17, 64, (5, 11, 17)),
+    (6, 30, 1, 64, (3, 5, 1)),
+    (8, 64, 33, 128, (3, 7, 33)),
     (1, 1, 9, 16, (1, 1, 9)),
     (9, 1, 1, 16, (5, 1, 1)),
 ])
