@@ -250,6 +250,13 @@ __device__ __forceinline__ int next_unit(const KernelParams& p, int u) {
     else return u + static_cast<int>(gridDim.x);
 }
 
+// The first unit of the head group after the one unit u belongs to.
+template <class C>
+__device__ __forceinline__ int next_group_unit(const KernelParams& p, int u) {
+    if constexpr (C::GROUPED) return (u | (p.hg - 1)) + 1 + (static_cast<int>(gridDim.x) - 1) * p.hg;
+    else return u + static_cast<int>(gridDim.x);
+}
+
 // Chunk order inside a unit: w-segment fastest, then h-row group, then frame.
 struct ChunkCursor {
     int kt, hc, wc;
@@ -869,10 +876,22 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
 
     int u = first_unit<C>(p);
     uint32_t gl = 0;   // local head-group counter (W-mask tiles)
-    Unit U{};          // the unit being processed, decoded when the previous one ends
+    Unit U{};          // the unit being processed
+    Unit Un{};         // mask instances: the next head group's first unit
+    // Mask tiles go out one head group ahead of use: a group's tile is
+    // published when the group two before it ends (that group's buffer is
+    // then free), so a group's first score tile never waits for the softmax
+    // to finish the previous group.
     if (u < p.n_units) {
         U = unit_of(p, u);
         if (!publish_qx(0, U)) return;
+        if constexpr (C::FAST) {
+            const int u1 = next_group_unit<C>(p, u);
+            if (u1 < p.n_units) {
+                Un = unit_of(p, u1);
+                if (!publish_qx(1, Un)) return;
+            }
+        }
     }
     // A finished unit's output is written once the next unit is set up, so its
     // last product completes meanwhile; then the tensor memory O is released.
@@ -1077,7 +1096,7 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
         }
 
         // this unit's output is written at the top of the next iteration, once
-        // the next unit is set up; its W masks go out now
+        // the next unit is set up
         const int64_t tok = ((static_cast<int64_t>(U.b) * p.Tq + t) * p.Hq + h) * p.Wq + w;
         if constexpr (C::WIDE)   // U.n counts (head, pass) pairs; a pass writes OB columns
             e_orow = p.out + (tok * p.NH + (U.n >> p.npass_log2)) * p.hd +
@@ -1091,9 +1110,18 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
         const bool new_group = group_end<C>(p, u);
         u = next_unit<C>(p, u);
         if (u < p.n_units) {
-            if (new_group) {   // another brick: decode it and publish its W masks
-                U = unit_of(p, u);
-                if (!publish_qx(++gl, U)) return;
+            if (new_group) {   // another brick (its mask tile is already out)
+                ++gl;
+                if constexpr (C::FAST) {
+                    U = Un;
+                    const int u2 = next_group_unit<C>(p, u);
+                    if (u2 < p.n_units) {   // the group after it, into the finished group's buffer
+                        Un = unit_of(p, u2);
+                        if (!publish_qx(gl + 1, Un)) return;
+                    }
+                } else {
+                    U = unit_of(p, u);
+                }
             } else {           // the next head of the same brick
                 ++U.n;
             }
