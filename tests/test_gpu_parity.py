@@ -80,6 +80,8 @@ FULL_CASES = [
     ((1, 3, 5, 40, 1, 512), (3, 3, 33)),     # HD 512 with per-key masks
     ((2, 3, 6, 12, 3, 1024), (3, 3, 5)),     # HD 1024: four passes, B and NH > 1
     ((1, 2, 4, 6, 1, 2048), (1, 3, 5)),      # HD 2048
+    ((1, 1, 2, 3, 1, 4096), (1, 1, 3)),      # HD 4096: sixteen passes
+    ((1, 2, 4, 40, 1, 1024), (1, 3, 33)),    # HD 1024 with per-key masks
     # whole-row W windows (KW = W): H windows applied by the tensor core
     ((1, 4, 10, 21, 2, 128), (3, 5, 21)),    # HD 128
     ((1, 5, 12, 9, 3, 32), (3, 3, 9)),       # HD 32
@@ -314,6 +316,7 @@ REGION_CASES = [
     ((1, 5, 9, 21, 2, 512), (3, 5, 7), (1, 2, 6, 3, 5, 9)),        # HD 512
     ((1, 5, 14, 25, 2, 64), (3, 5, 25), (1, 3, 0, 3, 8, 25)),      # whole-row W windows
     ((1, 5, 14, 25, 2, 64), (3, 5, 25), (0, 4, 5, 5, 7, 10)),      # whole-row W windows, W sub-box
+    ((2, 4, 11, 9, 3, 128), (3, 5, 9), (1, 3, 0, 2, 6, 9)),        # whole-row W windows, HD 128
     ((1, 4, 9, 50, 2, 64), (3, 3, 33), (0, 0, 7, 4, 9, 30)),       # wide window: per-key masks
 ]
 
