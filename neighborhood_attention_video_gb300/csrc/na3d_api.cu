@@ -83,13 +83,18 @@ struct Plan {
 };
 
 // Costs in units of score columns of a 128-row tile: every chunk costs its
-// tile width (tensor-core and exp work) plus a fixed overhead (barriers, mask
-// set-up, MMA issue); every brick adds the epilogue and its Q load. Columns of
-// the tensor-core W-mask path cost about half as much softmax work as columns
-// masked key by key.
-constexpr double kChunkOverhead = 24.0;
-constexpr double kBrickOverhead = 96.0;
+// tile width (tensor-core and exp work) plus a fixed overhead (the latency of
+// its score -> softmax -> product chain); every brick adds the unit boundary
+// (epilogue, last product, set-up: about 2.7 chunks of a 128-key tile on
+// GB300). Columns of the tensor-core mask paths cost about half as much
+// softmax work as columns masked key by key.
+constexpr double kChunkOverhead = 60.0;
+constexpr double kBrickOverhead = 250.0;
 constexpr double kFastColumn = 0.55;
+// Tensor-core work per tile column: the softmax works in 32-key words, the
+// MMAs in 16-key steps, so of two tiles with the same words the narrower
+// one is cheaper.
+constexpr double kMmaColumn = 0.05;
 
 // Row-mask plans (every W window is the whole axis): the tensor core masks
 // the H window through halo-row columns, so a brick's halo may span at most
@@ -97,7 +102,8 @@ constexpr double kFastColumn = 0.55;
 constexpr int64_t kRowsCols = 15;
 constexpr int64_t kRowsTiles = 5;
 
-Plan make_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap, bool allow_rows) {
+Plan make_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap, bool allow_rows,
+               bool allow_exact) {
     const int64_t H = ah.n, W = aw.n, KH = ah.k, KW = aw.k;
     Plan best;
     // mode 0: W windows by the tensor core (W unions up to 32 keys, a fixed
@@ -109,7 +115,11 @@ Plan make_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap, bool al
         const int64_t ew = (bw + KW - 1 < W) ? bw + KW - 1 : W;   // widest W union
         int64_t cwp = 0;
         if (mode == 1) cwp = 1;
-        else if (ew <= 32) cwp = ew <= 8 ? 8 : (ew <= 16 ? 16 : 32);
+        else if (ew <= 32) {
+            cwp = ew <= 8 ? 8 : (ew <= 16 ? 16 : 32);
+            // unions of 9 to 14 keys: rows of 12 or 14 keys where instances exist
+            if (allow_exact && ew > 8 && ew <= 14) cwp = ew <= 12 ? 12 : 14;
+        }
         const int64_t cw = cwp == 1 ? W : cwp ? cwp : (ew > ncap ? ncap : ew);
         const double col_cost = cwp ? kFastColumn : 1.0;
         int64_t nbw;
@@ -135,8 +145,10 @@ Plan make_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap, bool al
                     // the softmax works in 32-key words, so a tile costs its width
                     // rounded up to a word
                     const int64_t n_words = (n_mma + 31) / 32 * 32;
-                    const double cost = double(chunks) * (double(n_words) * col_cost + kChunkOverhead) +
-                                        double(bricks) * kBrickOverhead;
+                    const double cost =
+                        double(chunks) * (double(n_words) * col_cost + double(n_mma) * kMmaColumn +
+                                          kChunkOverhead) +
+                        double(bricks) * kBrickOverhead;
                     const bool better =
                         best.bt == 0 || cost < best.cost - 1e-9 ||
                         (cost < best.cost + 1e-9 && bw * bh * bt > int64_t(best.bw) * best.bh * best.bt);
@@ -157,19 +169,20 @@ Plan make_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap, bool al
 // Plans depend only on the grid, the query box, the window and the
 // score-tile cap; they are cached (bounded, mutex-guarded) because the search
 // takes ~0.1 ms.
-Plan cached_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap, bool allow_rows) {
+Plan cached_plan(const Axis& at, const Axis& ah, const Axis& aw, int ncap, bool allow_rows,
+                 bool allow_exact) {
     using Key = std::tuple<int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t,
-                           int64_t, int64_t, int64_t, int64_t, int, bool>;
+                           int64_t, int64_t, int64_t, int64_t, int, bool, bool>;
     static std::mutex mu;
     static std::map<Key, Plan> cache;
     const Key key{at.nq, at.off, at.n, at.k, ah.nq, ah.off, ah.n, ah.k,
-                  aw.nq, aw.off, aw.n, aw.k, ncap, allow_rows};
+                  aw.nq, aw.off, aw.n, aw.k, ncap, allow_rows, allow_exact};
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
-    Plan pl = make_plan(at, ah, aw, ncap, allow_rows);
+    Plan pl = make_plan(at, ah, aw, ncap, allow_rows, allow_exact);
     std::lock_guard<std::mutex> g(mu);
     if (cache.size() >= 1024) cache.clear();
     cache.emplace(key, pl);
@@ -268,7 +281,9 @@ int na3d_plan(int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD, int64_t K
     VariantInfo vi;
     if (!na3d::variant_info(int(HD), 0, &vi)) return NA3D_ERR_UNSUPPORTED;
     const bool rows = na3d::variant_info(int(HD), 1, nullptr);
-    const Plan pl = cached_plan(Axis{T, 0, T, KT}, Axis{H, 0, H, KH}, Axis{W, 0, W, KW}, vi.ncap, rows);
+    const bool exact = na3d::variant_info(int(HD), 12, nullptr) && na3d::variant_info(int(HD), 14, nullptr);
+    const Plan pl = cached_plan(Axis{T, 0, T, KT}, Axis{H, 0, H, KH}, Axis{W, 0, W, KW}, vi.ncap, rows,
+                                exact);
     if (!na3d::variant_info(int(HD), pl.cwp, &vi)) return NA3D_ERR_UNSUPPORTED;
     info->bt = pl.bt; info->bh = pl.bh; info->bw = pl.bw;
     info->cw = pl.cw; info->cr = pl.cr; info->n_mma = pl.n_mma;
@@ -328,7 +343,9 @@ int fwd_region(const void* q, const void* k, const void* v, void* out, int64_t B
     VariantInfo vi;
     if (!na3d::variant_info(int(HD), 0, &vi)) return NA3D_ERR_UNSUPPORTED;
     const bool rows = na3d::variant_info(int(HD), 1, nullptr);
-    const Plan pl = cached_plan(Axis{Tq, t0, T, KT}, Axis{Hq, h0, H, KH}, Axis{Wq, w0, W, KW}, vi.ncap, rows);
+    const bool exact = na3d::variant_info(int(HD), 12, nullptr) && na3d::variant_info(int(HD), 14, nullptr);
+    const Plan pl = cached_plan(Axis{Tq, t0, T, KT}, Axis{Hq, h0, H, KH}, Axis{Wq, w0, W, KW}, vi.ncap,
+                                rows, exact);
     if (!na3d::variant_info(int(HD), pl.cwp, &vi)) return NA3D_ERR_UNSUPPORTED;
 
     KernelParams kp;

@@ -80,6 +80,9 @@ struct Cfg {
     // index), Qx marks the halo rows outside each query's H window.
     static constexpr bool FAST = CWP > 0;
     static constexpr bool ROWS = CWP == 1;
+    // CWP 12 or 14: chunk rows of CWP keys that do not tile a 32-key word
+    // (exact fits of 11- to 14-key W unions, instead of padding them to 16)
+    static constexpr bool ODD = FAST && !ROWS && (CWP & (CWP - 1)) != 0;
     // softmax: columns per uniformly masked group (ROWS: 16, so that the
     // validity bits end at the tile width, a multiple of 16)
     static constexpr int RW = ROWS ? 16 : CWP;
@@ -101,7 +104,12 @@ struct Cfg {
     static constexpr int XSBO = 8 * XROWB;
     static constexpr int QX_TILE = 128 * XROWB;
     static constexpr int KX_TILE = NCAP * XROWB;
-    static constexpr int RPW = FAST ? 32 / RW : 0;   // uniformly masked groups per 32-column word
+    static constexpr int RPW = FAST && !ODD ? 32 / RW : 0;   // uniformly masked groups per 32-column word
+    static constexpr int NROWS = FAST ? (NCAP + RW - 1) / RW : 0;   // groups in a tile
+    // bits of the groups with a column in 32-column word q
+    static constexpr uint32_t word_rows(int q) {
+        return FAST ? ((0xFFFFFFFFu >> (31 - (32 * q + 31) / RW)) >> ((32 * q) / RW)) << ((32 * q) / RW) : 0u;
+    }
     static constexpr int HDB = HD < 64 ? HD : 64;   // head-dim columns per TMA box / smem row
     static constexpr int NREG = HD / HDB;           // boxes (smem regions) of a Q or K row (not WIDE)
     static constexpr int VREG = OB / HDB;           // boxes of a V row block (= NREG unless WIDE)
@@ -178,7 +186,9 @@ struct Cfg {
     static_assert(NCAP == 64 || NCAP == 128, "score tile width");
     static_assert(SW >= 64 || STEP == 2, "pairs of score words are adjacent in tensor memory");
     static_assert(NS >= 2 && NSV >= 2, "K/V rings need two stages");
-    static_assert(!FAST || (CWP == 1 || CWP == 8 || CWP == 16 || CWP == 32), "fast-path chunk stride");
+    static_assert(!FAST || (CWP == 1 || CWP == 8 || CWP == 12 || CWP == 14 || CWP == 16 || CWP == 32),
+                  "fast-path chunk stride");
+    static_assert(NROWS <= 32, "group bits");
     static_assert(!ROWS || (KEXT == 16 && !WIDE), "row-mask instances");
     static_assert(!WIDE || (CPS == 1 && HDB == 64 && OB == 256 && STEP == 2), "wide instances");
 };
@@ -759,6 +769,32 @@ __device__ __forceinline__ float fast_probabilities(const float* s, uint32_t row
     uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
     for (int q = 0; q < C::NW; ++q) {
+        if constexpr (C::ODD) {   // a row's keys may straddle words: the row of each pair is fixed
+            if (q * 32 < n_mma) {
+                uint32_t pk[16];
+                if (live[q]) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int i = (32 * q + 2 * j) / C::RW;   // both keys of a pair share a row
+                        const float nm = ((rowbits >> i) & 1u) ? -moff : -INFINITY;
+                        float e0, e1;
+                        f2_unpack(f2_fma(f2_pack(s[32 * q + 2 * j], s[32 * q + 2 * j + 1]), l2e2,
+                                         f2_pack(nm, nm)),
+                                  e0, e1);
+                        e0 = ex2_approx(e0);
+                        e1 = ex2_approx(e1);
+                        pk[j] = pack_bf16x2(e0, e1);
+                        if (j & 1) acc1 = f2_add(acc1, f2_pack(e0, e1));
+                        else acc0 = f2_add(acc0, f2_pack(e0, e1));
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) pk[j] = 0u;
+                }
+                tmem_st16(p_addr + q * 16, pk);
+            }
+            continue;
+        }
         if (q * 32 < n_mma) {
             uint32_t pk[16];
             if (live[q]) {
@@ -798,19 +834,34 @@ __device__ __forceinline__ float fast_probabilities(const float* s, uint32_t row
 template <class C>
 __device__ __forceinline__ float fast_row_max(const float* s, uint32_t rowbits, const bool* live) {
     float mx = -INFINITY;
+    if constexpr (C::ODD) {
+        float rm[C::NROWS];
 #pragma unroll
-    for (int q = 0; q < C::NW; ++q) {
-        if (live[q]) {
+        for (int i = 0; i < C::NROWS; ++i) rm[i] = -INFINITY;
 #pragma unroll
-            for (int rr = 0; rr < C::RPW; ++rr) {
-                const int i = q * C::RPW + rr;
-                float rm = -INFINITY;
+        for (int q = 0; q < C::NW; ++q) {
+            if (live[q]) {
 #pragma unroll
-                for (int jj = 0; jj < C::RW; jj += 2) {
-                    const int b = 32 * q + rr * C::RW + jj;
-                    rm = max3f(rm, s[b], s[b + 1]);
+                for (int b = 32 * q; b < 32 * q + 32; b += 2) rm[b / C::RW] = max3f(rm[b / C::RW], s[b], s[b + 1]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < C::NROWS; ++i) mx = ((rowbits >> i) & 1u) ? fmaxf(mx, rm[i]) : mx;
+    } else {
+#pragma unroll
+        for (int q = 0; q < C::NW; ++q) {
+            if (live[q]) {
+#pragma unroll
+                for (int rr = 0; rr < C::RPW; ++rr) {
+                    const int i = q * C::RPW + rr;
+                    float rm = -INFINITY;
+#pragma unroll
+                    for (int jj = 0; jj < C::RW; jj += 2) {
+                        const int b = 32 * q + rr * C::RW + jj;
+                        rm = max3f(rm, s[b], s[b + 1]);
+                    }
+                    mx = ((rowbits >> i) & 1u) ? fmaxf(mx, rm) : mx;
                 }
-                mx = ((rowbits >> i) & 1u) ? fmaxf(mx, rm) : mx;
             }
         }
     }
@@ -990,7 +1041,8 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
 #pragma unroll
             for (int q = 0; q < C::NW; ++q) {
                 bool mine;
-                if constexpr (C::FAST) mine = (rowbits >> (q * C::RPW)) & ((1u << C::RPW) - 1u);
+                if constexpr (C::ODD) mine = (rowbits & C::word_rows(q)) != 0u;
+                else if constexpr (C::FAST) mine = (rowbits >> (q * C::RPW)) & ((1u << C::RPW) - 1u);
                 else mine = m[q] != 0u;
                 live[q] = (q * 32 < p.n_mma) && __any_sync(0xffffffffu, mine);
             }
@@ -1206,6 +1258,20 @@ na3d_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
+    // The score ring starts as zeros: a tile narrower than its last 32-column
+    // word leaves columns that the softmax reads (and masks) unwritten, and
+    // fresh tensor memory may hold any bit pattern.
+    if (warp < 4) {
+        float z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0.f;
+        for (uint32_t c = C::TM_R; c + 32 <= C::TM_COLS; c += 32)
+            tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, z);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 
     if (warp < 4) {
         if (C::CPS == 2) regs_increase<C::REGS_HIGH>();
@@ -1250,8 +1316,9 @@ static void info_t(VariantInfo* v) {
 }
 
 // The instance table: (HD, score-tile cap, K/V stages, CTAs per SM) x chunk
-// stride CWP (0: generic masks; 8, 16, 32: W window applied by the tensor core;
-// 1: whole-row W windows, H window applied by the tensor core).
+// stride CWP (0: generic masks; 8, 16, 32 and, for HD 64 and 128, 12 and 14: W
+// window applied by the tensor core; 1: whole-row W windows, H window applied
+// by the tensor core).
 #define NA3D_HD_TABLE(X, CWP) \
     X(16, 128, 4, 2, CWP)     \
     X(32, 128, 3, 2, CWP)     \
@@ -1259,6 +1326,11 @@ static void info_t(VariantInfo* v) {
     X(128, 64, 2, 2, CWP)     \
     X(256, 64, 2, 1, CWP)     \
     X(512, 64, 4, 1, CWP)
+#define NA3D_EXACT_TABLE(X)  \
+    X(64, 128, 2, 2, 12)     \
+    X(64, 128, 2, 2, 14)     \
+    X(128, 64, 2, 2, 12)     \
+    X(128, 64, 2, 2, 14)
 #define NA3D_ROWS_TABLE(X)  \
     X(16, 128, 4, 2, 1)     \
     X(32, 128, 3, 2, 1)     \
@@ -1266,7 +1338,8 @@ static void info_t(VariantInfo* v) {
     X(128, 64, 2, 2, 1)     \
     X(256, 64, 2, 1, 1)
 #define NA3D_VARIANTS(X) \
-    NA3D_HD_TABLE(X, 0) NA3D_HD_TABLE(X, 8) NA3D_HD_TABLE(X, 16) NA3D_HD_TABLE(X, 32) NA3D_ROWS_TABLE(X)
+    NA3D_HD_TABLE(X, 0) NA3D_HD_TABLE(X, 8) NA3D_HD_TABLE(X, 16) NA3D_HD_TABLE(X, 32) NA3D_ROWS_TABLE(X) \
+    NA3D_EXACT_TABLE(X)
 
 bool variant_info(int hd, int cwp, VariantInfo* info) {
     if (hd > 256) hd = 512;   // the wide instance serves every HD >= 512

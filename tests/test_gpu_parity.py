@@ -82,6 +82,11 @@ FULL_CASES = [
     ((1, 2, 4, 6, 1, 2048), (1, 3, 5)),      # HD 2048
     ((1, 1, 2, 3, 1, 4096), (1, 1, 3)),      # HD 4096: sixteen passes
     ((1, 2, 4, 40, 1, 1024), (1, 3, 33)),    # HD 1024 with per-key masks
+    # rows of 12 or 14 keys (W unions of 9 to 14 keys without padding to 16)
+    ((1, 6, 16, 14, 2, 64), (3, 3, 5)),      # HD 64, 14-key rows
+    ((1, 6, 16, 40, 2, 64), (3, 3, 5)),      # HD 64, 12-key rows
+    ((1, 6, 16, 14, 2, 128), (3, 3, 5)),     # HD 128, 12-key rows
+    ((1, 6, 16, 20, 2, 128), (3, 3, 5)),     # HD 128, 14-key rows
     # whole-row W windows (KW = W): H windows applied by the tensor core
     ((1, 4, 10, 21, 2, 128), (3, 5, 21)),    # HD 128
     ((1, 5, 12, 9, 3, 32), (3, 3, 9)),       # HD 32
@@ -215,7 +220,8 @@ def test_deterministic_and_stream_independent():
                                           ((2, 8, 48, 48, 8, 128), (3, 7, 7)),
                                           ((1, 8, 32, 40, 8, 256), (3, 5, 7)),
                                           ((1, 6, 24, 40, 8, 512), (3, 5, 7)),
-                                          ((2, 8, 64, 33, 8, 64), (3, 7, 33))],
+                                          ((2, 8, 64, 33, 8, 64), (3, 7, 33)),
+                                          ((1, 16, 48, 48, 8, 64), (11, 11, 11))],
                          ids=lambda x: "x".join(map(str, x)))
 def test_repeated_launches_are_bit_identical(shape, kernel):
     """Shapes with many work units per CTA: every per-chunk pipeline barrier

@@ -154,6 +154,18 @@ def test_qkv_proj_validation(lib):
     assert call(x, w, qkv + 64, qkv, 10, 64, 2, 32) == ERR_ALIAS  # bias inside qkv
 
 
+@pytest.mark.parametrize("shape,kernel,stride", [
+    ((1, 6, 16, 14, 2, 64), (3, 3, 5), 14), ((1, 6, 16, 40, 2, 64), (3, 3, 5), 12),
+    ((1, 6, 16, 14, 2, 128), (3, 3, 5), 12), ((1, 6, 16, 20, 2, 128), (3, 3, 5), 14),
+    ((1, 16, 48, 48, 8, 64), (11, 11, 11), 14),
+])
+def test_w_unions_of_nine_to_fourteen_keys_get_exact_rows(lib, shape, kernel, stride):
+    """W unions of 9 to 14 keys run with rows of 12 or 14 keys (no padding to
+    16); the shapes the GPU parity tests use for those instances."""
+    p = na.na3d_plan(*shape[1:], *kernel)
+    assert p["w_stride"] == stride and p["cw"] == stride
+
+
 def test_every_power_of_two_head_dim_is_planned(lib):
     """HD > 256 is served by one wide instance: 64-key tiles, 64-column boxes."""
     for hd in (512, 1024, 2048, 4096):
