@@ -105,6 +105,31 @@ def test_parity_whole_output(shape, kernel):
     check(got, want, f"{shape} {kernel}")
 
 
+def random_cases(n, seed):
+    """Seeded random problems over every mask mode: grids up to 16 x 24 x 60,
+    odd windows (a quarter of them spanning the whole W axis), head dims 16
+    to 512, one or two batches and heads."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        T, H = (int(x) for x in rng.integers(1, 17, size=2))
+        W = int(rng.integers(1, 61))
+        KT, KH, KW = (int(rng.choice(np.arange(1, N + 1, 2))) for N in (T, H, W))
+        if W % 2 == 1 and rng.random() < 0.25:
+            KW = W
+        HD = int(rng.choice([16, 32, 64, 64, 128, 128, 256, 512]))
+        B, NH = (int(x) for x in rng.integers(1, 3, size=2))
+        out.append(((B, T, H, W, NH, HD), (KT, KH, KW)))
+    return out
+
+
+@pytest.mark.parametrize("shape,kernel", random_cases(32, 2024), ids=lambda x: "x".join(map(str, x)))
+def test_parity_random_problems(shape, kernel):
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=sum(shape) + sum(kernel))
+    got = run_gpu(q, k, v, kernel)
+    check(got, oracle.na3d_fwd(q, k, v, kernel), f"random {shape} {kernel}")
+
+
 # ------------------------------------------------------------ full sizes, sampled rows
 
 def sample_rows(shape, n_random, seed=0):
