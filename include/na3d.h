@@ -46,7 +46,7 @@ enum na3d_status {
     NA3D_ERR_ARCH = 8,           /* the current device is not compute capability 10.3 */
     NA3D_ERR_CUDA = 9,           /* a CUDA runtime or driver call failed */
     NA3D_ERR_DEVICE_TIMEOUT = 10, /* a pipeline wait inside the kernel gave up */
-    NA3D_ERR_UNSUPPORTED = 11    /* valid but not implemented (HD > 256) */
+    NA3D_ERR_UNSUPPORTED = 11    /* valid but not implemented (no current argument returns it) */
 };
 
 /*
@@ -67,7 +67,9 @@ enum na3d_status {
  *   read only and may alias one another; out must not overlap any of them.
  * B: batch size, T, H, W: grid sizes, NH: heads, all >= 1 (a size < 1,
  *   including an empty batch, returns NA3D_ERR_SHAPE).
- * HD: head dimension, a power of two >= 16 (above 256: NA3D_ERR_UNSUPPORTED).
+ * HD: head dimension, a power of two >= 16, with NH*HD < 2^31 (else
+ *   NA3D_ERR_OVERFLOW). Above 256 the output is computed in passes of 256
+ *   columns that recompute the same scores (slower per column, same result).
  * KT, KH, KW: odd window lengths with 1 <= KT <= T, 1 <= KH <= H, 1 <= KW <= W.
  * stream: a cudaStream_t on the current device (NULL = legacy default stream).
  *
@@ -201,8 +203,9 @@ typedef struct na3d_plan_info {
     int64_t bricks_per_slice;     /* bricks per (batch, head) slice */
     int64_t chunks_per_slice;     /* chunks per (batch, head) slice */
     int64_t smem_bytes;           /* dynamic shared memory per CTA */
-    int32_t w_stride;             /* 8, 16 or 32: chunk rows padded to this many keys and the
-                                     W window applied by the tensor core; 1: every W window
+    int32_t w_stride;             /* 8, 12, 14, 16 or 32: chunk rows padded to this many keys
+                                     and the W window applied by the tensor core (12 and 14
+                                     for HD 64 and 128 only); 1: every W window
                                      is the whole axis (KW == W), chunk rows are whole grid
                                      rows and the H window is applied by the tensor core;
                                      0: per-key masks */
