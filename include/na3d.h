@@ -78,7 +78,10 @@ enum na3d_status {
  * argument error returns its code before anything is enqueued (out is not
  * written). NA3D_ERR_CUDA reports a failed launch or descriptor encoding.
  * Faults inside the kernel surface through the stream as usual; a pipeline
- * wait that gives up is reported by na3d_device_status().
+ * wait that gives up is reported by na3d_device_status(). The launch may be
+ * captured into a CUDA graph on `stream` (the tensor maps are passed by
+ * value and the plan is chosen at capture time); replays read the buffers
+ * the call was given. na3d_device_status synchronizes and cannot be captured.
  */
 int na3d_fwd(const void* q, const void* k, const void* v, void* out,
              int64_t B, int64_t T, int64_t H, int64_t W, int64_t NH, int64_t HD,
