@@ -195,7 +195,7 @@ const char* na3d_status_string(int status);
  * cores), and each brick streams the union of its queries' windows (its halo)
  * through shared memory in chunks of cr rows (consecutive h) of cw keys
  * (consecutive w) in one frame t. The scores of a chunk form one
- * 128 x n_mma tile.
+ * 128 x n_mma tile (n_mma <= tile_cap).
  */
 typedef struct na3d_plan_info {
     int32_t bt, bh, bw;           /* query brick */
@@ -212,7 +212,10 @@ typedef struct na3d_plan_info {
                                      is the whole axis (KW == W), chunk rows are whole grid
                                      rows and the H window is applied by the tensor core;
                                      0: per-key masks */
-    int32_t reserved;
+    int32_t tile_cap;             /* score-tile capacity of the kernel instance: 128 (HD <= 64) or
+                                     64 (HD >= 128), or 96 for the HD-64 instances whose score
+                                     tiles are double-buffered (the next one is computed while
+                                     the softmax works on the current one) */
 } na3d_plan_info;
 
 /*

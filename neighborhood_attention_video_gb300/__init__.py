@@ -48,7 +48,7 @@ class PlanInfo(ctypes.Structure):
                 ("hd_box", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("bricks_per_slice", ctypes.c_int64), ("chunks_per_slice", ctypes.c_int64),
                 ("smem_bytes", ctypes.c_int64), ("w_stride", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("tile_cap", ctypes.c_int32)]
 
 
 def library_path() -> str:

@@ -183,7 +183,7 @@ struct Cfg {
     static_assert(NSLOT >= 3 && TM_R + NSLOT * SW <= TM_COLS && OPIECES * 32 <= OCOLS, "TMEM ring");
     static_assert(LAG <= RING, "a product barrier never runs a phase ahead of its waiter");
     static_assert(SMEM_ALLOC * CPS <= 232448 && SMEM_ALLOC <= 232448, "shared memory budget");
-    static_assert(NCAP == 64 || NCAP == 128, "score tile width");
+    static_assert(NCAP == 64 || NCAP == 96 || NCAP == 128, "score tile width");
     static_assert(SW >= 64 || STEP == 2, "pairs of score words are adjacent in tensor memory");
     static_assert(NS >= 2 && NSV >= 2, "K/V rings need two stages");
     static_assert(!FAST || (CWP == 1 || CWP == 8 || CWP == 12 || CWP == 14 || CWP == 16 || CWP == 32),
@@ -1064,7 +1064,8 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
                 if (q * 32 < p.n_mma) {
                     uint32_t sl = slot + (32u * q) / C::SW;
                     sl = sl >= static_cast<uint32_t>(C::NSLOT) ? sl - C::NSLOT : sl;
-                    tmem_ld64(t_row + C::TM_R + sl * C::SW + (32u * q) % C::SW, s + 32 * q);
+                    if (q + 1 < C::NW) tmem_ld64(t_row + C::TM_R + sl * C::SW + (32u * q) % C::SW, s + 32 * q);
+                    else tmem_ld32(t_row + C::TM_R + sl * C::SW + (32u * q) % C::SW, s + 32 * q);
                 }
             }
 
@@ -1318,7 +1319,10 @@ static void info_t(VariantInfo* v) {
 // The instance table: (HD, score-tile cap, K/V stages, CTAs per SM) x chunk
 // stride CWP (0: generic masks; 8, 16, 32 and, for HD 64 and 128, 12 and 14: W
 // window applied by the tensor core; 1: whole-row W windows, H window applied
-// by the tensor core).
+// by the tensor core). HD 64 has a second family of 96-key score tiles: O and
+// four 48-column slots fill the CTA's 256 tensor-memory columns, and the
+// slots are used as pairs, so the next score tile is computed while the
+// softmax works on the current one.
 #define NA3D_HD_TABLE(X, CWP) \
     X(16, 128, 4, 2, CWP)     \
     X(32, 128, 3, 2, CWP)     \
@@ -1331,6 +1335,13 @@ static void info_t(VariantInfo* v) {
     X(64, 128, 2, 2, 14)     \
     X(128, 64, 2, 2, 12)     \
     X(128, 64, 2, 2, 14)
+#define NA3D_PAIRED_TABLE(X)  \
+    X(64, 96, 3, 2, 0)     \
+    X(64, 96, 3, 2, 8)     \
+    X(64, 96, 3, 2, 12)    \
+    X(64, 96, 3, 2, 14)    \
+    X(64, 96, 3, 2, 16)    \
+    X(64, 96, 3, 2, 32)
 #define NA3D_ROWS_TABLE(X)  \
     X(16, 128, 4, 2, 1)     \
     X(32, 128, 3, 2, 1)     \
@@ -1339,12 +1350,14 @@ static void info_t(VariantInfo* v) {
     X(256, 64, 2, 1, 1)
 #define NA3D_VARIANTS(X) \
     NA3D_HD_TABLE(X, 0) NA3D_HD_TABLE(X, 8) NA3D_HD_TABLE(X, 16) NA3D_HD_TABLE(X, 32) NA3D_ROWS_TABLE(X) \
-    NA3D_EXACT_TABLE(X)
+    NA3D_EXACT_TABLE(X) NA3D_PAIRED_TABLE(X)
 
-bool variant_info(int hd, int cwp, VariantInfo* info) {
+int default_ncap(int hd) { return hd <= 64 ? 128 : 64; }
+
+bool variant_info(int hd, int cwp, int ncap, VariantInfo* info) {
     if (hd > 256) hd = 512;   // the wide instance serves every HD >= 512
 #define X(hd_, n_, s_, c_, w_)                   \
-    if (hd == hd_ && cwp == w_) {                \
+    if (hd == hd_ && cwp == w_ && ncap == n_) {  \
         if (info) info_t<hd_, n_, s_, c_, w_>(info); \
         return true;                             \
     }
@@ -1353,12 +1366,12 @@ bool variant_info(int hd, int cwp, VariantInfo* info) {
     return false;
 }
 
-cudaError_t launch_fwd(int hd, int cwp, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_fwd(int hd, int cwp, int ncap, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const KernelParams& kp, int grid,
                        cudaStream_t stream) {
     if (hd > 256) hd = 512;
 #define X(hd_, n_, s_, c_, w_) \
-    if (hd == hd_ && cwp == w_) return launch_t<hd_, n_, s_, c_, w_>(tq, tk, tv, kp, grid, stream);
+    if (hd == hd_ && cwp == w_ && ncap == n_) return launch_t<hd_, n_, s_, c_, w_>(tq, tk, tv, kp, grid, stream);
     NA3D_VARIANTS(X)
 #undef X
     return cudaErrorInvalidValue;

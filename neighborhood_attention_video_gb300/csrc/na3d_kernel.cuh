@@ -59,13 +59,15 @@ struct VariantInfo {
 };
 
 // Instances exist for HD in {16, 32, 64, 128, 256, >= 512 (one instance for
-// every larger power of two)} and chunk stride cwp in {0 (generic per-key
-// masks), 8, 16, 32 (W window applied by the tensor core)}.
-// (info may be null: then only whether the instance exists)
-bool variant_info(int hd, int cwp, VariantInfo* info);
+// every larger power of two)}, chunk stride cwp in {0 (generic per-key masks),
+// 8, 12, 14, 16, 32 (W window applied by the tensor core), 1 (H window applied
+// by the tensor core)} and score-tile cap ncap (default_ncap(hd), and 96 for
+// HD 64: paired tiles). info may be null: then only whether it exists.
+int default_ncap(int hd);
+bool variant_info(int hd, int cwp, int ncap, VariantInfo* info);
 
-// Launch the instance for (hd, cwp) on `stream` with `grid` persistent CTAs.
-cudaError_t launch_fwd(int hd, int cwp, const CUtensorMap& tq, const CUtensorMap& tk,
+// Launch the instance for (hd, cwp, ncap) on `stream` with `grid` persistent CTAs.
+cudaError_t launch_fwd(int hd, int cwp, int ncap, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const KernelParams& kp, int grid,
                        cudaStream_t stream);
 

@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import na3d_inputs
+from instance_cases import INSTANCE_CASES
 import neighborhood_attention_video_gb300 as na
 import oracle
 
@@ -82,11 +83,6 @@ FULL_CASES = [
     ((1, 2, 4, 6, 1, 2048), (1, 3, 5)),      # HD 2048
     ((1, 1, 2, 3, 1, 4096), (1, 1, 3)),      # HD 4096: sixteen passes
     ((1, 2, 4, 40, 1, 1024), (1, 3, 33)),    # HD 1024 with per-key masks
-    # rows of 12 or 14 keys (W unions of 9 to 14 keys without padding to 16)
-    ((1, 6, 16, 14, 2, 64), (3, 3, 5)),      # HD 64, 14-key rows
-    ((1, 6, 16, 40, 2, 64), (3, 3, 5)),      # HD 64, 12-key rows
-    ((1, 6, 16, 14, 2, 128), (3, 3, 5)),     # HD 128, 12-key rows
-    ((1, 6, 16, 20, 2, 128), (3, 3, 5)),     # HD 128, 14-key rows
     # whole-row W windows (KW = W): H windows applied by the tensor core
     ((1, 4, 10, 21, 2, 128), (3, 5, 21)),    # HD 128
     ((1, 5, 12, 9, 3, 32), (3, 3, 9)),       # HD 32
@@ -94,7 +90,7 @@ FULL_CASES = [
     ((1, 4, 20, 3, 2, 16), (3, 7, 3)),       # HD 16, W = 3
     ((2, 6, 30, 1, 2, 64), (3, 5, 1)),       # W = KW = 1
     ((1, 7, 40, 17, 2, 64), (5, 11, 17)),    # tall H windows: many h-chunks per brick
-]
+] + [(shape, kernel) for shape, kernel, _, _ in INSTANCE_CASES]   # one problem per kernel instance
 
 
 @pytest.mark.parametrize("shape,kernel", FULL_CASES, ids=lambda x: "x".join(map(str, x)))

@@ -10,6 +10,7 @@ import pytest
 
 import neighborhood_attention_video_gb300 as na
 from neighborhood_attention_video_gb300 import build as na_build
+from instance_cases import INSTANCE_CASES
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "na3d.h")
@@ -154,16 +155,16 @@ def test_qkv_proj_validation(lib):
     assert call(x, w, qkv + 64, qkv, 10, 64, 2, 32) == ERR_ALIAS  # bias inside qkv
 
 
-@pytest.mark.parametrize("shape,kernel,stride", [
-    ((1, 6, 16, 14, 2, 64), (3, 3, 5), 14), ((1, 6, 16, 40, 2, 64), (3, 3, 5), 12),
-    ((1, 6, 16, 14, 2, 128), (3, 3, 5), 12), ((1, 6, 16, 20, 2, 128), (3, 3, 5), 14),
-    ((1, 16, 48, 48, 8, 64), (11, 11, 11), 14),
+@pytest.mark.parametrize("shape,kernel,cap,stride", INSTANCE_CASES + [
+    ((1, 16, 48, 48, 8, 64), (11, 11, 11), 128, 14),
 ])
-def test_w_unions_of_nine_to_fourteen_keys_get_exact_rows(lib, shape, kernel, stride):
-    """W unions of 9 to 14 keys run with rows of 12 or 14 keys (no padding to
-    16); the shapes the GPU parity tests use for those instances."""
+def test_each_instance_is_selected_by_its_problem(lib, shape, kernel, cap, stride):
+    """The problems the GPU parity tests use to exercise each kernel instance
+    do select that instance (score-tile cap and W row stride)."""
     p = na.na3d_plan(*shape[1:], *kernel)
-    assert p["w_stride"] == stride and p["cw"] == stride
+    assert (p["tile_cap"], p["w_stride"]) == (cap, stride)
+    if stride not in (0, 1):
+        assert p["cw"] == stride
 
 
 def test_every_power_of_two_head_dim_is_planned(lib):
@@ -215,7 +216,8 @@ def check_plan_covers_windows(T, H, W, HD, kernel):
     KT, KH, KW = kernel
     p = na.na3d_plan(T, H, W, 1, HD, *kernel)
     bt, bh, bw, cw, cr = p["bt"], p["bh"], p["bw"], p["cw"], p["cr"]
-    ncap = 64 if HD >= 128 else 128
+    ncap = p["tile_cap"]
+    assert ncap == (64 if HD >= 128 else 128) or (HD == 64 and ncap == 96)
     assert 1 <= bt * bh * bw <= 128
     assert cr * cw <= ncap and p["n_mma"] % 16 == 0 and cr * cw <= p["n_mma"] <= ncap
     assert max(bt, bh, bw, cw, cr) <= 256
