@@ -167,6 +167,23 @@ def test_each_instance_is_selected_by_its_problem(lib, shape, kernel, cap, strid
         assert p["cw"] == stride
 
 
+@pytest.mark.parametrize("grid,kernel,cap,brick", [
+    ((16, 64, 96), (3, 5, 5), 96, (4, 8, 4)),      # same plan in both families: paired tiles
+    ((36, 64, 96), (3, 5, 5), 96, (4, 8, 4)),
+    ((16, 64, 64), (3, 7, 7), 128, (2, 8, 8)),     # the 96-key cap would force 2x10x6 bricks
+    ((16, 48, 48), (11, 11, 11), 128, (4, 8, 4)),  # ... or 16x4x2 bricks
+    ((16, 32, 32), (7, 7, 7), 128, (8, 8, 2)),
+    ((4, 8, 128), (3, 5, 27), 128, (4, 8, 4)),     # ... or 3 rows of 32 keys instead of 4
+])
+def test_paired_tiles_only_where_they_keep_the_plan(lib, grid, kernel, cap, brick):
+    """HD 64: the 96-key paired family is chosen when its plan costs no more
+    than the 128-key family's (the same plan runs faster on paired tiles; a
+    plan the smaller cap forces measured slower)."""
+    p = na.na3d_plan(*grid, 8, 64, *kernel)
+    assert p["tile_cap"] == cap
+    assert (p["bt"], p["bh"], p["bw"]) == brick
+
+
 def test_every_power_of_two_head_dim_is_planned(lib):
     """HD > 256 is served by one wide instance: 64-key tiles, 64-column boxes."""
     for hd in (512, 1024, 2048, 4096):
