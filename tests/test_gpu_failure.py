@@ -25,6 +25,7 @@ def to_dev(a):
     ((1, 4, 8, 16, 2, 32), (3, 5, 5)),     # W window by the tensor core
     ((1, 4, 8, 5, 2, 64), (3, 5, 5)),      # whole-row W windows: H window by the tensor core
     ((1, 5, 9, 40, 2, 64), (3, 5, 33)),    # per-key masks
+    ((1, 6, 12, 16, 3, 64), (3, 1, 3)),    # HD 64, 96-key score tiles in pairs of slots
     ((1, 2, 4, 6, 1, 512), (1, 3, 5)),     # HD 512: Q and K streamed per region
 ], ids=lambda x: "x".join(map(str, x)))
 def test_withheld_load_is_reported_and_the_device_stays_usable(shape, kernel):

@@ -237,6 +237,7 @@ def test_deterministic_and_stream_independent():
 
 
 @pytest.mark.parametrize("shape,kernel", [((1, 16, 64, 64, 8, 64), (3, 7, 7)),
+                                          ((1, 16, 64, 96, 8, 64), (3, 5, 5)),   # paired 96-key tiles
                                           ((1, 16, 64, 5, 8, 64), (3, 5, 5)),
                                           ((2, 8, 48, 48, 8, 128), (3, 7, 7)),
                                           ((1, 8, 32, 40, 8, 256), (3, 5, 7)),
@@ -265,18 +266,19 @@ def test_repeated_launches_are_bit_identical(shape, kernel):
             np.testing.assert_array_equal(got, first)
 
 
-def test_concurrent_launches_on_two_streams():
-    """Two launches in flight at once on different streams (an HD-64 and an
-    HD-128 problem, several units per CTA): their CTAs may share SMs and the
-    tensor memory of an SM. Each result equals its launch alone, bit for bit,
-    and the device reports no wait that ran out."""
-    cases = [((1, 8, 32, 48, 4, 64), (3, 7, 7), 41), ((1, 6, 24, 40, 4, 128), (3, 5, 7), 42)]
+def test_concurrent_launches_on_several_streams():
+    """Launches in flight at once on different streams (HD-64 problems on
+    both tile families and an HD-128 problem, several units per CTA): their
+    CTAs may share SMs and the tensor memory of an SM. Each result equals its
+    launch alone, bit for bit, and the device reports no wait that ran out."""
+    cases = [((1, 8, 32, 48, 4, 64), (3, 7, 7), 41), ((1, 6, 24, 40, 4, 128), (3, 5, 7), 42),
+             ((1, 8, 32, 48, 4, 64), (3, 5, 5), 43)]
     alone, dev = [], []
     for shape, kernel, seed in cases:
         q, k, v = na3d_inputs.make_qkv(*shape, seed=seed)
         alone.append(run_gpu(q, k, v, kernel))
         dev.append((to_dev(q), to_dev(k), to_dev(v), kernel))
-    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    streams = [torch.cuda.Stream() for _ in cases]
     for _ in range(3):
         outs = [torch.full_like(d[0], float("nan")) for d in dev]
         torch.cuda.synchronize()
