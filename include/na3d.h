@@ -213,7 +213,7 @@ typedef struct na3d_plan_info {
                                      rows and the H window is applied by the tensor core;
                                      0: per-key masks */
     int32_t tile_cap;             /* score-tile capacity of the kernel instance: 128 (HD <= 64) or
-                                     64 (HD >= 128), or 96 for the HD-64 instances whose score
+                                     64 (HD >= 128), or 96 for the HD <= 64 instances whose score
                                      tiles are double-buffered (the next one is computed while
                                      the softmax works on the current one) */
 } na3d_plan_info;

@@ -1319,10 +1319,10 @@ static void info_t(VariantInfo* v) {
 // The instance table: (HD, score-tile cap, K/V stages, CTAs per SM) x chunk
 // stride CWP (0: generic masks; 8, 16, 32 and, for HD 64 and 128, 12 and 14: W
 // window applied by the tensor core; 1: whole-row W windows, H window applied
-// by the tensor core). HD 64 has a second family of 96-key score tiles: O and
-// four 48-column slots fill the CTA's 256 tensor-memory columns, and the
-// slots are used as pairs, so the next score tile is computed while the
-// softmax works on the current one.
+// by the tensor core). HD <= 64 has a second family of 96-key score tiles: O
+// (64 columns) and four 48-column slots fill the CTA's 256 tensor-memory
+// columns, and the slots are used as pairs, so the next score tile is
+// computed while the softmax works on the current one.
 #define NA3D_HD_TABLE(X, CWP) \
     X(16, 128, 4, 2, CWP)     \
     X(32, 128, 3, 2, CWP)     \
@@ -1336,6 +1336,14 @@ static void info_t(VariantInfo* v) {
     X(128, 64, 2, 2, 12)     \
     X(128, 64, 2, 2, 14)
 #define NA3D_PAIRED_TABLE(X)  \
+    X(16, 96, 4, 2, 0)     \
+    X(16, 96, 4, 2, 8)     \
+    X(16, 96, 4, 2, 16)    \
+    X(16, 96, 4, 2, 32)    \
+    X(32, 96, 3, 2, 0)     \
+    X(32, 96, 3, 2, 8)     \
+    X(32, 96, 3, 2, 16)    \
+    X(32, 96, 3, 2, 32)    \
     X(64, 96, 3, 2, 0)     \
     X(64, 96, 3, 2, 8)     \
     X(64, 96, 3, 2, 12)    \

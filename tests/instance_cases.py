@@ -24,4 +24,13 @@ INSTANCE_CASES = [
     ((1, 7, 17, 5, 2, 64), (1, 1, 1), 96, 8),
     ((1, 7, 11, 19, 2, 64), (3, 1, 9), 96, 32),
     ((1, 3, 8, 50, 2, 64), (1, 7, 33), 96, 0),
+    # HD 16 and 32, 96-key tiles in pairs of slots
+    ((1, 3, 5, 50, 2, 16), (3, 3, 33), 96, 0),
+    ((1, 5, 11, 13, 2, 16), (3, 1, 1), 96, 8),
+    ((1, 7, 7, 19, 2, 16), (3, 1, 7), 96, 16),
+    ((1, 7, 5, 40, 2, 16), (3, 1, 9), 96, 32),
+    ((2, 3, 5, 50, 2, 32), (3, 3, 33), 96, 0),
+    ((1, 5, 11, 13, 2, 32), (3, 1, 1), 96, 8),
+    ((1, 7, 7, 19, 2, 32), (3, 1, 7), 96, 16),
+    ((1, 7, 5, 40, 2, 32), (3, 1, 9), 96, 32),
 ]

@@ -234,7 +234,7 @@ def check_plan_covers_windows(T, H, W, HD, kernel):
     p = na.na3d_plan(T, H, W, 1, HD, *kernel)
     bt, bh, bw, cw, cr = p["bt"], p["bh"], p["bw"], p["cw"], p["cr"]
     ncap = p["tile_cap"]
-    assert ncap == (64 if HD >= 128 else 128) or (HD == 64 and ncap == 96)
+    assert ncap == (64 if HD >= 128 else 128) or (HD <= 64 and ncap == 96)
     assert 1 <= bt * bh * bw <= 128
     assert cr * cw <= ncap and p["n_mma"] % 16 == 0 and cr * cw <= p["n_mma"] <= ncap
     assert max(bt, bh, bw, cw, cr) <= 256
