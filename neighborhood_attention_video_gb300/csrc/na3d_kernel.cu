@@ -976,6 +976,19 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
             if (!swait(sy.bar(C::B_OFULL), e_ul & 1u)) return;
             tc_fence_after();
             const float inv = (e_valid && e_l > 0.f) ? rcp_approx(e_l) : 0.f;
+            // HD >= 128 (a 32-byte aligned output): lanes 2i and 2i + 1 store rows 2i and 2i + 1
+            // together, so each store instruction writes 64 contiguous bytes per row
+            // instead of 32 scattered ones (fewer, larger write requests)
+            bool paired = false;
+            const bool odd = (lane & 1) != 0;
+            uint16_t* p_orow = nullptr;   // the partner lane's row
+            bool p_valid = false;
+            if constexpr (C::HD >= 128) {
+                paired = p.out_v8 != 0;
+                p_orow = reinterpret_cast<uint16_t*>(
+                    __shfl_xor_sync(0xffffffffu, reinterpret_cast<unsigned long long>(e_orow), 1));
+                p_valid = __shfl_xor_sync(0xffffffffu, e_valid ? 1 : 0, 1) != 0;
+            }
 #pragma unroll 1
             for (int q = 0; q < C::OPIECES; ++q) {
                 float o[32];
@@ -984,7 +997,23 @@ __device__ void softmax_role(const KernelParams& p, const Sync& sy, uint32_t bas
                 uint32_t pk[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(o[2 * j] * inv, o[2 * j + 1] * inv);
-                if (e_valid) {
+                if (paired) {
+                    // even lane: the first 32 bytes of its row, then of the odd partner's row;
+                    // odd lane: the last 32 bytes of the even partner's row, then of its row
+                    uint32_t snd[8], rcv[8], d1[8], d2[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) snd[j] = odd ? pk[j] : pk[8 + j];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) rcv[j] = __shfl_xor_sync(0xffffffffu, snd[j], 1);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        d1[j] = odd ? rcv[j] : pk[j];
+                        d2[j] = odd ? pk[8 + j] : rcv[j];
+                    }
+                    const int off = odd ? 16 : 0;
+                    if (odd ? p_valid : e_valid) st_global_v8((odd ? p_orow : e_orow) + q * 32 + off, d1);
+                    if (odd ? e_valid : p_valid) st_global_v8((odd ? e_orow : p_orow) + q * 32 + off, d2);
+                } else if (e_valid) {
                     constexpr int kBytes = (C::HD < 32 ? C::HD : 32) * 2;   // bytes per piece
                     if (p.out_v8) {   // whole 32-byte sectors per lane
 #pragma unroll
