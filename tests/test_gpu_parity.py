@@ -210,6 +210,24 @@ def test_score_spike_in_a_later_chunk(kernel, hd):
     check(got, oracle.na3d_fwd(q, k, v, kernel), f"spike {shape} {kernel}")
 
 
+@pytest.mark.parametrize("shape,kernel", [
+    ((1, 6, 8, 16, 2, 64), (3, 3, 3)),     # tensor-core W mask, 16-key rows
+    ((1, 6, 8, 48, 2, 64), (3, 3, 33)),    # per-key masks, 48-key rows
+    ((1, 6, 8, 48, 2, 32), (3, 3, 33)),    # HD 32
+], ids=lambda x: "x".join(map(str, x)))
+def test_score_spike_on_paired_score_tiles(shape, kernel):
+    """The score spike on problems that run on the 96-key tiles in pairs of
+    tensor-memory slots (two tiles in flight): the rescale of O waits for the
+    previous product through that ring's barriers."""
+    assert na.na3d_plan(*shape[1:], *kernel)["tile_cap"] == 96
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=17)
+    kf = na3d_inputs.bf16_bits_to_f64(k)
+    kf[:, 4:] *= 40.0
+    k = na3d_inputs.f64_to_bf16_bits(kf)
+    got = run_gpu(q, k, v, kernel)
+    check(got, oracle.na3d_fwd(q, k, v, kernel), f"spike {shape} {kernel}")
+
+
 def test_score_spike_with_whole_row_windows():
     """As above, with KW = W: the H window comes from the tensor core, and
     the spiking rows must still raise the kept reference maximum."""
@@ -377,6 +395,7 @@ REGION_CASES = [
     ((1, 5, 14, 25, 2, 64), (3, 5, 25), (0, 4, 5, 5, 7, 10)),      # whole-row W windows, W sub-box
     ((2, 4, 11, 9, 3, 128), (3, 5, 9), (1, 3, 0, 2, 6, 9)),        # whole-row W windows, HD 128
     ((1, 4, 9, 50, 2, 64), (3, 3, 33), (0, 0, 7, 4, 9, 30)),       # wide window: per-key masks
+    ((1, 6, 16, 40, 2, 64), (3, 5, 5), (1, 2, 8, 4, 12, 24)),      # interior box, HD 64 (3,5,5)
 ]
 
 
