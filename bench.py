@@ -377,7 +377,7 @@ def run_ours(args):
             "kernel": list(kernel),
             "l2": "flushed between timed steps (2x L2 buffer overwritten)",
             "parallelism": "replicas" if world > 1 else "single GPU",
-            "plan": {k2: plan[k2] for k2 in ("bt", "bh", "bw", "cw", "cr", "n_mma")},
+            "plan": {k2: plan[k2] for k2 in ("bt", "bh", "bw", "cw", "cr", "n_mma", "tile_cap", "w_stride")},
         },
         "roofline": {
             "bound": terms["bound"],
@@ -471,7 +471,9 @@ def per_config_table(dev, stream, flush, peaks, resident=None, steps=20, warmup=
             "us_warm": t_warm * 1e6,
             "executed_tflops": executed / t / 1e12,
             "executed_over_useful": executed / useful_flops(shape, kernel),
-            "plan": [plan["bt"], plan["bh"], plan["bw"], plan["cw"], plan["cr"], plan["n_mma"]],
+            # brick bt x bh x bw, chunk rows cr of cw keys, tile width n_mma, tile cap, W row stride
+            "plan": [plan["bt"], plan["bh"], plan["bw"], plan["cw"], plan["cr"], plan["n_mma"],
+                     plan["tile_cap"], plan["w_stride"]],
             "traffic": ncu_traffic(name),
             "inputs": "seeded recipe, seed 0",
         }
