@@ -13,7 +13,7 @@ import ctypes
 import os
 
 __all__ = [
-    "NA3DError", "NA3DUnavailable", "na3d_fwd", "na3d_fwd_strided", "na3d_fwd_region",
+    "NA3DError", "NA3DUnavailable", "na3d_attention", "na3d_fwd", "na3d_fwd_strided", "na3d_fwd_region",
     "na3d_qkv_proj", "qkv_views", "na3d_status_string", "na3d_plan",
     "na3d_device_status", "library_path", "load_library", "EXPORTED_SYMBOLS",
 ]
@@ -144,6 +144,16 @@ def na3d_fwd(q, k, v, out, kernel_size, stream=None) -> None:
                       *shape, KT, KH, KW, _stream_handle(stream))
     if rc != NA3D_OK:
         raise NA3DError(rc, "na3d_fwd")
+
+
+def na3d_attention(q, k, v, kernel_size, stream=None):
+    """Returns a new tensor out = NA3D(q, k, v): ``na3d_fwd`` with the output
+    allocated like ``q`` (contiguous bf16 (B, T, H, W, NH, HD) on its device).
+    q must already be scaled by HD**-0.5."""
+    torch = _torch_module()
+    out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    na3d_fwd(q, k, v, out, kernel_size, stream=stream)
+    return out
 
 
 def _token_stride(name, t) -> int:

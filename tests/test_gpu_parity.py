@@ -338,6 +338,16 @@ def test_cuda_graph_capture_and_replay():
     np.testing.assert_array_equal(from_dev(out), run_gpu(q2, k2, v2, kernel))
 
 
+def test_attention_returns_what_na3d_fwd_writes():
+    shape, kernel = (1, 6, 20, 36, 2, 64), (3, 7, 7)
+    q, k, v = na3d_inputs.make_qkv(*shape, seed=23)
+    want = run_gpu(q, k, v, kernel)
+    out = na.na3d_attention(to_dev(q), to_dev(k), to_dev(v), kernel)
+    torch.cuda.synchronize()
+    assert out.shape == shape and out.dtype == torch.bfloat16 and out.is_contiguous()
+    np.testing.assert_array_equal(from_dev(out), want)
+
+
 def test_invalid_device_arguments_are_rejected():
     shape = (1, 4, 8, 16, 2, 32)
     x = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
