@@ -160,6 +160,54 @@ def test_parity_full_size_sampled(shape, kernel):
     check(got[rows], want, f"{shape} {kernel} ({rows.size} sampled rows)")
 
 
+def test_parity_beyond_2_31_elements():
+    """Tensors of more than 2^31 elements (6 GB each): every offset past 2^31
+    must be computed in 64 bits. The inputs are drawn on the device (seeded).
+    Each sampled row, including the last rows of the tensor, is checked by the
+    oracle on its own window box: a (1, KT, KH, KW, 1, HD) problem whose
+    windows cover the whole box, so its output there is the whole-grid one."""
+    shape, kernel = (2, 79, 192, 192, 8, 64), (3, 5, 5)
+    B, T, H, W, NH, HD = shape
+    KT, KH, KW = kernel
+    n = int(np.prod(shape))
+    assert n > 2 ** 31
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(31)
+
+    def draw(scale):
+        t = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+        flat = t.view(-1)
+        step = 1 << 28
+        for i in range(0, n, step):
+            m = min(step, n - i)
+            flat[i:i + m] = (torch.randn(m, generator=gen, device="cuda") * scale).to(torch.bfloat16)
+        return t
+
+    q, k, v = draw(HD ** -0.5), draw(1.0), draw(1.0)
+    out = torch.full_like(q, float("nan"))
+    na.na3d_fwd(q, k, v, out, kernel)
+    torch.cuda.synchronize()
+    assert na.na3d_device_status() == 0
+
+    total = B * T * H * W * NH
+    rng = np.random.default_rng(5)
+    rows = sorted(set(rng.integers(0, total, size=200).tolist()) | set(range(total - 40, total)) | {0})
+    got, want = [], []
+    for r in rows:
+        b, t, h, w, head = (int(x) for x in np.unravel_index(r, (B, T, H, W, NH)))
+        sT, sH, sW = (oracle.window_start(i, K, N) for i, K, N in ((t, KT, T), (h, KH, H), (w, KW, W)))
+        box = (b, slice(sT, sT + KT), slice(sH, sH + KH), slice(sW, sW + KW), head)
+        kb = from_dev(k[box].contiguous()).reshape(1, KT, KH, KW, 1, HD)
+        vb = from_dev(v[box].contiguous()).reshape(1, KT, KH, KW, 1, HD)
+        qb = np.zeros_like(kb)
+        qb[0, t - sT, h - sH, w - sW, 0] = from_dev(q[b, t, h, w, head].contiguous())
+        want.append(oracle.na3d_fwd(qb, kb, vb, kernel)[0, t - sT, h - sH, w - sW, 0])
+        got.append(from_dev(out[b, t, h, w, head].contiguous()))
+    check(np.stack(got), np.stack(want), f"{shape} {kernel} ({len(rows)} sampled rows, last ones included)")
+    del q, k, v, out
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------ exact special cases
 
 def test_unit_window_returns_v_bit_exactly():
