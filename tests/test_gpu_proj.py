@@ -88,6 +88,32 @@ def test_full_size_projection_on_sampled_rows():
     check_projection(got[rows], x[rows], w, b, NH, HD, f"proj M={M} sampled {rows.size} rows")
 
 
+def test_projection_beyond_2_31_output_elements():
+    """The benchmark's own projection shape (393216 tokens, C = 2048, 16 heads of
+    128): 2.4e9 output elements, so the last rows sit past 2^31. x is drawn on
+    the device (seeded); the oracle checks the first and last tiles and a
+    random sample of rows from their x rows."""
+    M, C, NH, HD = 393216, 2048, 16, 128
+    N = 3 * NH * HD
+    assert M * N > 2 ** 31
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(9)
+    xd = torch.randn((M, C), generator=gen, device="cuda").to(torch.bfloat16)
+    _, w, b = make(8, C, NH, HD, seed=10, with_bias=True)
+    qkv = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    na.na3d_qkv_proj(xd, to_dev(w), to_dev(b), qkv, NH, HD)
+    torch.cuda.synchronize()
+    assert na.na3d_device_status() == 0
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([np.arange(128), np.arange(M - 128, M), rng.integers(0, M, 512)]))
+    idx = torch.from_numpy(rows).cuda()
+    got = from_dev(qkv.index_select(0, idx))
+    x_rows = from_dev(xd.index_select(0, idx))
+    check_projection(got, x_rows, w, b, NH, HD, f"proj M={M} C={C}: sampled {rows.size} rows")
+    del xd, qkv
+    torch.cuda.empty_cache()
+
+
 def test_unaligned_output_uses_16_byte_stores():
     M, C, NH, HD = 513, 128, 2, 64
     x, w, b = make(M, C, NH, HD, seed=5, with_bias=True)
